@@ -9,7 +9,8 @@ import importlib
 
 __all__ = [
     "sort_keys", "sort_pairs", "compact_positive", "segmented_sort_",
-    "digit_histograms", "GsortError", "library_path", "build",
+    "digit_histograms", "GsortError", "library_path",
+    "radix_workspace_bytes", "compact_workspace_bytes",
 ]
 
 

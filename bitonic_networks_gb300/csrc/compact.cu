@@ -1,0 +1,211 @@
+// compact.cu -- stream compaction of the positive floats, the 1-bit special
+// case of the radix sort's scatter ([CUDA3] "Stream Compaction": predicate,
+// exclusive scan of the predicate, scatter; single pass with decoupled
+// look-back and a warp-wide look-back window).
+//
+// One kernel reads every tile once: predicate, block scan of the per-thread
+// counts, publish the tile count, look back (warp 0 inspects 32 earlier tiles
+// per step), stage the kept values of the tile contiguously in shared memory
+// and copy them out as one run.  The last tile records the total m; a second
+// kernel writes +0.0 to out[m..n) (the pages' worked example shows a zero
+// tail; their kernels leave it unwritten).  Traffic: read 4n, write 4n.
+#include <algorithm>
+
+#include "gsort_internal.cuh"
+
+namespace gsort {
+namespace {
+
+constexpr int kCompactThreads = 512;
+constexpr int kCompactItems = 16;          // per thread, a multiple of 4
+constexpr uint32_t kCompactTile = kCompactThreads * kCompactItems;
+
+__global__ void k_zero_words(uint32_t *p, uint32_t nwords) {
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < nwords;
+         i += gridDim.x * blockDim.x)
+        p[i] = 0;
+}
+
+// x > 0 under IEEE comparison, on the bit pattern: sign clear, not +0, not
+// NaN (0 < bits <= 0x7F800000).  Positive subnormals count as positive.
+__device__ __forceinline__ uint32_t is_positive(uint32_t bits) {
+    return (bits - 1u) < 0x7F800000u ? 1u : 0u;
+}
+
+template <int T, int IPT>
+__global__ void __launch_bounds__(T)
+k_compact(const uint32_t *__restrict__ in, uint32_t *__restrict__ out, uint32_t n,
+          uint32_t *states, uint32_t *tile_counter, uint32_t *status, uint32_t *abort_flag,
+          unsigned long long *kept, uint32_t num_tiles, uint32_t spin_limit,
+          uint32_t stall_tile, int vec_ok) {
+    constexpr uint32_t TILE = T * IPT;
+    constexpr int WARPS = T / 32;
+    __shared__ uint32_t s_buf[TILE];
+    __shared__ uint32_t s_warp[WARPS];
+    __shared__ uint32_t s_misc[4];
+
+    const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        s_misc[0] = atomicAdd(tile_counter, 1u);
+        s_misc[1] = ld_relaxed(abort_flag);
+    }
+    __syncthreads();
+    const uint32_t tile = s_misc[0];
+    if (s_misc[1]) return;
+    const uint32_t base = tile * TILE;
+    const uint32_t tile_n = min(TILE, n - base);
+
+    // blocked arrangement: thread t owns items [t*IPT, t*IPT + IPT) of the tile
+    uint32_t x[IPT];
+    const uint32_t first = tid * IPT;
+    if (tile_n == TILE && vec_ok) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(in + base + first);
+#pragma unroll
+        for (int q = 0; q < IPT / 4; ++q) {
+            const uint4 v = __ldcs(src + q);
+            x[4 * q + 0] = v.x;
+            x[4 * q + 1] = v.y;
+            x[4 * q + 2] = v.z;
+            x[4 * q + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < IPT; ++j) x[j] = (first + j < tile_n) ? in[base + first + j] : 0u;
+    }
+    uint32_t flags = 0;
+#pragma unroll
+    for (int j = 0; j < IPT; ++j) flags |= is_positive(x[j]) << j;
+    const uint32_t cnt = __popc(flags);
+
+    // block exclusive scan of the per-thread counts
+    const uint32_t incl = warp_inclusive_scan(cnt, lane);
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t w = lane < WARPS ? s_warp[lane] : 0u;
+        const uint32_t wi = warp_inclusive_scan(w, lane);
+        if (lane < WARPS) s_warp[lane] = wi - w;
+        if (lane == WARPS - 1) s_misc[2] = wi;   // tile total
+    }
+    __syncthreads();
+    const uint32_t total = s_misc[2];
+    uint32_t pos = s_warp[warp] + incl - cnt;
+
+    // decoupled look-back by warp 0: lane l inspects tile (t - 1 - l)
+    if (warp == 0) {
+        uint32_t prefix = 0;
+        bool ok = true;
+        if (lane == 0 && tile != stall_tile)
+            st_relaxed(states + tile, (tile == 0 ? kFlagPrefix : kFlagAgg) | total);
+        if (tile > 0 && tile != stall_tile) {
+            int32_t t = static_cast<int32_t>(tile) - 1 - static_cast<int32_t>(lane);
+            uint32_t polls = 0, ns = 32;
+            while (true) {
+                // before tile 0 sits an empty prefix
+                const uint32_t s = (t >= 0) ? ld_relaxed(states + t) : kFlagPrefix;
+                const uint32_t flag = s & ~kValueMask;
+                const uint32_t pmask = __ballot_sync(kFullMask, flag == kFlagPrefix);
+                const uint32_t zmask = __ballot_sync(kFullMask, flag == 0);
+                // lanes up to and including the nearest published prefix matter
+                const uint32_t need = pmask ? (((pmask & (0u - pmask)) << 1) - 1u) : kFullMask;
+                if (zmask & need) {
+                    ++polls;
+                    const bool give_up = __any_sync(kFullMask, polls >= spin_limit ||
+                                                                   ld_relaxed(abort_flag) != 0);
+                    if (give_up) { ok = false; break; }
+                    backoff(ns);
+                    continue;
+                }
+                prefix += __reduce_add_sync(kFullMask, ((need >> lane) & 1u) ? (s & kValueMask) : 0u);
+                if (pmask) break;
+                t -= 32;
+            }
+            if (ok && lane == 0) st_relaxed(states + tile, kFlagPrefix | (prefix + total));
+        }
+        if (lane == 0) {
+            s_misc[1] = ok ? 0u : 1u;
+            s_misc[3] = prefix;
+            if (!ok) record_error(status, abort_flag, GSORT_ETIMEOUT);
+        }
+    }
+    __syncthreads();
+    if (s_misc[1] || tile == stall_tile) return;
+    const uint32_t prefix = s_misc[3];
+
+    // stage the kept values contiguously, then copy them out as one run
+#pragma unroll
+    for (int j = 0; j < IPT; ++j)
+        if ((flags >> j) & 1u) s_buf[pos++] = x[j];
+    __syncthreads();
+    for (uint32_t i = tid; i < total; i += T) {
+        const uint32_t g = prefix + i;
+        if (g < n) out[g] = s_buf[i];
+    }
+    if (tile == num_tiles - 1 && tid == 0) *kept = static_cast<unsigned long long>(prefix) + total;
+}
+
+// +0.0 into out[m..n), m read from the workspace; also reports m.
+__global__ void k_zero_tail(uint32_t *out, uint32_t n, const unsigned long long *kept,
+                            int64_t *num_kept) {
+    const uint32_t m = static_cast<uint32_t>(min(*kept, static_cast<unsigned long long>(n)));
+    if (blockIdx.x == 0 && threadIdx.x == 0 && num_kept != nullptr)
+        *num_kept = static_cast<int64_t>(m);
+    const uint32_t gtid = blockIdx.x * blockDim.x + threadIdx.x;
+    const uint32_t gstride = gridDim.x * blockDim.x;
+    // head up to a 16-byte boundary, vector body, tail
+    uint32_t head = static_cast<uint32_t>(((16 - (reinterpret_cast<uintptr_t>(out + m) & 15)) & 15) >> 2);
+    head = min(head, n - m);
+    const uint32_t nvec = (n - m - head) >> 2;
+    uint4 *vec = reinterpret_cast<uint4 *>(out + m + head);
+    for (uint32_t v = gtid; v < nvec; v += gstride) __stcs(vec + v, make_uint4(0, 0, 0, 0));
+    if (gtid < head) out[m + gtid] = 0;
+    const uint32_t tail0 = m + head + nvec * 4;
+    if (gtid < n - tail0) out[tail0 + gtid] = 0;
+}
+
+void record(cudaEvent_t *ev, int num, int idx, cudaStream_t s) {
+    if (ev != nullptr && idx < num && ev[idx] != nullptr) cudaEventRecord(ev[idx], s);
+}
+
+}  // namespace
+
+CompactLayout compact_layout(uint32_t n) {
+    CompactLayout L{};
+    L.tiles = (n + kCompactTile - 1) / kCompactTile;
+    L.states = kHdrBytes;
+    L.total = kHdrBytes + align_up(static_cast<size_t>(L.tiles) * sizeof(uint32_t), kWsAlign);
+    return L;
+}
+
+int launch_compact(const CompactLaunch &L) {
+    const CompactLayout lay = compact_layout(L.n);
+    cudaStream_t s = L.stream;
+    uint32_t *words = reinterpret_cast<uint32_t *>(L.ws);
+    uint32_t *status = reinterpret_cast<uint32_t *>(L.ws + kHdrStatus);
+    uint32_t *abort_flag = reinterpret_cast<uint32_t *>(L.ws + kHdrAbort);
+    uint32_t *counter = reinterpret_cast<uint32_t *>(L.ws + kHdrCounters);
+    unsigned long long *kept = reinterpret_cast<unsigned long long *>(L.ws + kHdrKept);
+    uint32_t *states = reinterpret_cast<uint32_t *>(L.ws + lay.states);
+
+    record(L.events, L.num_events, 0, s);
+    const uint32_t init_words = static_cast<uint32_t>(kHdrBytes / 4) + lay.tiles;
+    const uint32_t init_grid = std::min<uint32_t>((init_words + 1023) / 1024, 4u * L.sm_count);
+    k_zero_words<<<init_grid, 256, 0, s>>>(words, init_words);
+    if (cudaGetLastError() != cudaSuccess) return GSORT_ECUDA;
+    record(L.events, L.num_events, 1, s);
+
+    const int vec_ok = (reinterpret_cast<uintptr_t>(L.in) & 15) == 0;
+    k_compact<kCompactThreads, kCompactItems><<<lay.tiles, kCompactThreads, 0, s>>>(
+        L.in, L.out, L.n, states, counter, status, abort_flag, kept, lay.tiles, L.spin_limit,
+        L.stall_tile, vec_ok);
+    if (cudaGetLastError() != cudaSuccess) return GSORT_ECUDA;
+    record(L.events, L.num_events, 2, s);
+
+    const uint32_t tail_grid = std::max(1u, std::min<uint32_t>((L.n / 4 + 255) / 256, 8u * L.sm_count));
+    k_zero_tail<<<tail_grid, 256, 0, s>>>(L.out, L.n, kept, L.num_kept);
+    if (cudaGetLastError() != cudaSuccess) return GSORT_ECUDA;
+    record(L.events, L.num_events, 3, s);
+    return GSORT_OK;
+}
+
+}  // namespace gsort

@@ -1,0 +1,163 @@
+// Internal declarations of libgsort: workspace layout, look-back state
+// encoding, device primitives and the host launchers each .cu file defines.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "gsort.h"
+
+namespace gsort {
+
+// ----------------------------------------------------------- workspace header
+// Byte offsets from the start of every workspace.  The header is cleared by
+// the init kernel at the start of each call.
+constexpr size_t kHdrStatus = 0;      // u32: 0, or a gsort_status a kernel recorded
+constexpr size_t kHdrAbort = 4;       // u32: non-zero once a wait gave up; later tiles bail out
+constexpr size_t kHdrCounters = 128;  // u32 tile counters, one per 128-byte line
+constexpr int kNumCounters = 8;
+constexpr size_t kHdrKept = kHdrCounters + 128 * kNumCounters;  // u64 kept count (compaction)
+constexpr size_t kHdrHist = 2048;     // u32[4][256] digit histograms (radix)
+constexpr size_t kHdrBytes = 8192;    // header size, keeps what follows 256-byte aligned
+constexpr size_t kWsAlign = 256;
+
+// ------------------------------------------------------------ look-back words
+// One 32-bit word per (tile[, digit]): 2 flag bits and a 30-bit count.
+// 0 = nothing published yet; AGG = the tile's own count; PREFIX = the count
+// over this tile and every earlier tile ([CUDA3] decoupled look-back: three
+// states per block).  The 30-bit field is why n <= 2^30 - 1.
+constexpr uint32_t kFlagAgg = 1u << 30;
+constexpr uint32_t kFlagPrefix = 2u << 30;
+constexpr uint32_t kValueMask = (1u << 30) - 1;
+constexpr uint32_t kDefaultSpinLimit = 1u << 20;  // polls; with back-off about a second
+constexpr uint32_t kNoStall = 0xFFFFFFFFu;
+
+// Smallest tile of any digit-pass variant; sizes the look-back regions.
+constexpr uint32_t kMinRadixTile = 4096;
+
+constexpr uint32_t kFullMask = 0xFFFFFFFFu;
+
+// ------------------------------------------------------------------ helpers
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed(uint32_t *p, uint32_t v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Order-preserving map of float bit patterns to unsigned integers: negative
+// values have every bit flipped, non-negative values only the sign bit
+// ([PMPP10] section 8, exercise 7; IEEE totalOrder for non-NaN values).
+__device__ __forceinline__ uint32_t float_key_in(uint32_t bits) {
+    return bits ^ (static_cast<uint32_t>(static_cast<int32_t>(bits) >> 31) | 0x80000000u);
+}
+
+// Inverse of float_key_in.
+__device__ __forceinline__ uint32_t float_key_out(uint32_t u) {
+    return u ^ (((u >> 31) - 1u) | 0x80000000u);
+}
+
+// Inclusive warp scan (Kogge-Stone over shuffles).
+__device__ __forceinline__ uint32_t warp_inclusive_scan(uint32_t v, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        uint32_t t = __shfl_up_sync(kFullMask, v, o);
+        if (lane >= o) v += t;
+    }
+    return v;
+}
+
+// Records a device-side error once and raises the abort flag.
+__device__ __forceinline__ void record_error(uint32_t *status, uint32_t *abort_flag, int code) {
+    atomicCAS(status, 0u, static_cast<uint32_t>(code));
+    atomicExch(abort_flag, 1u);
+}
+
+// Back-off between polls of a look-back word.
+__device__ __forceinline__ void backoff(uint32_t &ns) {
+    __nanosleep(ns);
+    if (ns < 1024) ns <<= 1;
+}
+
+// -------------------------------------------------------- host-side helpers
+struct DeviceInfo {
+    int device;
+    int sm_count;
+};
+int device_info(DeviceInfo *out);  // returns GSORT_OK or GSORT_ECUDA
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ------------------------------------------------------------ launch plans
+struct RadixLaunch {
+    const uint32_t *keys_in;
+    uint32_t *keys_out;
+    const uint32_t *vals_in;  // null: keys only
+    uint32_t *vals_out;
+    uint32_t n;
+    int kind;
+    int begin_bit, end_bit;
+    unsigned char *ws;
+    uint32_t spin_limit;
+    uint32_t stall_tile;
+    cudaEvent_t *events;
+    int num_events;
+    int variant;
+    cudaStream_t stream;
+    int sm_count;
+};
+
+// Layout of the radix workspace after the header.
+struct RadixLayout {
+    uint32_t tiles_max;   // look-back rows per region
+    size_t look_a, look_b;
+    size_t tmp_keys, tmp_vals;
+    size_t total;
+};
+RadixLayout radix_layout(uint32_t n, bool with_values);
+
+int radix_num_variants();
+const char *radix_variant_name(int v);
+uint32_t radix_variant_tile(int v);
+
+// Launchers (each returns GSORT_OK or GSORT_ECUDA).
+int launch_radix(const RadixLaunch &L);
+int launch_digit_histograms(const uint32_t *keys, uint32_t n, int kind, int begin_bit,
+                            int end_bit, uint32_t *hist_out, cudaStream_t stream, int sm_count);
+
+struct CompactLayout {
+    uint32_t tiles;
+    size_t states;
+    size_t total;
+};
+CompactLayout compact_layout(uint32_t n);
+
+struct CompactLaunch {
+    const uint32_t *in;
+    uint32_t *out;
+    uint32_t n;
+    int64_t *num_kept;
+    unsigned char *ws;
+    uint32_t spin_limit;
+    uint32_t stall_tile;
+    cudaEvent_t *events;
+    int num_events;
+    cudaStream_t stream;
+    int sm_count;
+};
+int launch_compact(const CompactLaunch &L);
+
+int launch_segmented_bitonic(uint32_t *keys, int64_t num_segments, int segment_len,
+                             cudaStream_t stream);
+
+}  // namespace gsort

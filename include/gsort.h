@@ -1,0 +1,204 @@
+/*
+ * gsort.h -- C ABI of libgsort.so: GB300 (sm_103a) stable LSD radix sort,
+ * stream compaction and segmented bitonic sort.
+ *
+ * Sources of the operations (reference pages, by title and section):
+ *   [PMPP10]  "Parallel Patterns: Sorting on the GPU" (textbook chapter 10):
+ *             10.2 Bitonic Sort, 10.3 Radix Sort, 10.6 Key-Value sorting,
+ *             10.7 stable vs unstable sorting, section 8 exercises.
+ *   [CUDA3]   "CUDA 算子笔记 3" (CUDA operator notes 3): Stream Compaction
+ *             (three kernels; decoupled look-back), Radix Sort (CPU LSD
+ *             sort; processing several bits at once: histogram of every
+ *             pass, scan of the bins, one-pass scatter with look-back).
+ *   [WGPU41]  "WebGPU Unleashed 4.1 Radix Sort": key/id pair buffers,
+ *             stable per-digit reordering.
+ *   [GPUSORT] "gpu排序" (GPU sort): bitonic sort of <=1024 keys per block,
+ *             padded with 0xFFFFFFFF.
+ *
+ * Conventions shared by every call:
+ *   - Pointers named d_* are DEVICE pointers on the current CUDA device.
+ *     The caller owns every buffer, including the workspace; the library
+ *     never allocates or frees memory and keeps no state between calls.
+ *   - Every call is asynchronous on `stream` (0 = legacy default stream).
+ *     Argument errors and launch errors are returned at once.  Errors that
+ *     only the device can see (a look-back wait that gave up) are recorded
+ *     in the workspace and returned by gsort_check().
+ *   - 32-bit data must be 4-byte aligned (else GSORT_EALIGN).  Buffers that
+ *     are also 16-byte aligned take 128-bit vector paths; others take a
+ *     scalar path with identical results.
+ *   - n counts elements.  0 <= n <= GSORT_MAX_N (larger: GSORT_ETOOBIG);
+ *     n == 0 is a no-op returning GSORT_OK.  The cap comes from the 30-bit
+ *     count field of the look-back state words.
+ *   - Workspaces must be 256-byte aligned (torch and cudaMalloc allocations
+ *     are).  Their contents on entry do not matter.  Two calls that share a
+ *     workspace must not run concurrently.
+ */
+#ifndef GSORT_H
+#define GSORT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same definition as the CUDA runtime's, so either header may come first. */
+typedef struct CUstream_st *cudaStream_t;
+
+typedef enum gsort_status {
+    GSORT_OK = 0,
+    GSORT_EINVAL = -1,      /* bad argument: NULL, bad range, overlapping buffers */
+    GSORT_EALIGN = -2,      /* a pointer is not 4-byte (data) or 256-byte (workspace) aligned */
+    GSORT_EWORKSPACE = -3,  /* workspace missing or smaller than the *_workspace_bytes() answer */
+    GSORT_ETOOBIG = -4,     /* n > GSORT_MAX_N */
+    GSORT_ECUDA = -5,       /* a CUDA runtime call or kernel launch failed */
+    GSORT_ETIMEOUT = -6     /* a device-side look-back wait gave up (see gsort_check) */
+} gsort_status;
+
+typedef enum gsort_key_kind {
+    GSORT_KEY_U32 = 0,      /* unsigned 32-bit integers */
+    GSORT_KEY_F32 = 1       /* IEEE-754 binary32, ordered as totalOrder for non-NaN */
+} gsort_key_kind;
+
+#define GSORT_MAX_N ((int64_t)((1 << 30) - 1))
+
+/* Human-readable name of a status code (static string). */
+const char *gsort_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int gsort_version(void);
+
+/* ------------------------------------------------------------------------
+ * Radix sort  ([PMPP10] 10.3, 10.6, 10.7; [CUDA3] Radix Sort, several bits
+ * at once; [WGPU41])
+ *
+ * Stable LSD radix sort with 8-bit digits, least significant digit first.
+ * One upfront pass reads the keys once and builds the 256-bin histogram of
+ * every digit; each digit pass then scatters every element to
+ *   (keys with a smaller digit) + (keys with this digit in earlier tiles)
+ *   + (its stable rank among this digit's keys in its own tile),
+ * where the middle term comes from a decoupled look-back over per-(tile,
+ * digit) counts.  Equal keys keep their input order; values move with keys.
+ *
+ * Float keys (GSORT_KEY_F32): the bit pattern is mapped to an unsigned
+ * integer that orders every non-NaN value as IEEE totalOrder (-inf < ... <
+ * -0 < +0 < ... < +inf); the output holds the original bit patterns.
+ * ([PMPP10] section 8, exercise 7 poses the question; this is the reading
+ * taken.)  NaNs are not promised an order; with this map +NaN sorts after
+ * +inf and -NaN before -inf.
+ * ---------------------------------------------------------------------- */
+
+/* Workspace bytes for sorting n elements (with_values != 0: pairs).
+ * Holds a status word, counters, the digit histograms, two look-back
+ * state regions and one ping-pong buffer per sorted array. */
+size_t gsort_radix_workspace_bytes(int64_t n, int with_values);
+
+/* Sort n keys ascending by all 32 bits.  d_keys_in is not modified unless
+ * it equals d_keys_out (in place is allowed).  Partially overlapping
+ * buffers: GSORT_EINVAL. */
+int gsort_radix_keys(const void *d_keys_in, void *d_keys_out, int64_t n,
+                     int kind, void *d_ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Stable sort of (key, value) pairs by key bits [begin_bit, end_bit)
+ * (0 <= begin_bit <= end_bit <= 32).  Bits outside the range do not take
+ * part in the order but are carried.  begin_bit == end_bit copies.  For
+ * kind == GSORT_KEY_F32 the range applies to the mapped key (use 0..32).
+ * d_vals_in and d_vals_out are both NULL (keys only) or both non-NULL.
+ * In-place (in == out) is allowed for keys and for values. */
+int gsort_radix_pairs(const void *d_keys_in, void *d_keys_out,
+                      const uint32_t *d_vals_in, uint32_t *d_vals_out, int64_t n,
+                      int kind, int begin_bit, int end_bit,
+                      void *d_ws, size_t ws_bytes, cudaStream_t stream);
+
+/* The upfront histogram step on its own: d_hist_out receives
+ * passes * 256 uint32 counts, passes = ceil((end_bit - begin_bit) / 8);
+ * entry [p * 256 + d] counts the keys whose p-th 8-bit digit (from
+ * begin_bit, last digit narrowed to end_bit) is d.  Needs no workspace. */
+int gsort_digit_histograms(const void *d_keys, int64_t n, int kind,
+                           int begin_bit, int end_bit, uint32_t *d_hist_out,
+                           cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Stream compaction  ([CUDA3] Stream Compaction: predicate, exclusive scan,
+ * scatter; the single-pass decoupled look-back version)
+ *
+ * Writes every d_in[i] > 0 (IEEE: NaN, +0 and -0 are dropped, positive
+ * subnormals kept) to d_out[0..m) in input order and +0.0 to d_out[m..n).
+ * If d_num_kept is not NULL, *d_num_kept = m (device int64) on completion.
+ * d_in and d_out must not overlap.
+ * ---------------------------------------------------------------------- */
+size_t gsort_compact_workspace_bytes(int64_t n);
+
+int gsort_compact_positive(const float *d_in, float *d_out, int64_t n,
+                           int64_t *d_num_kept, void *d_ws, size_t ws_bytes,
+                           cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Segmented bitonic sort  ([GPUSORT] sort of <=1024 elements in one block;
+ * [PMPP10] 10.2)
+ *
+ * Sorts each of num_segments consecutive segments of segment_len uint32
+ * keys ascending, in place, with the bitonic network held in registers
+ * (one warp per segment).  1 <= segment_len <= 1024; lengths that are not a
+ * power of two are padded internally with 0xFFFFFFFF.  num_segments >= 0.
+ * Not stable (keys only, so the result is still unique).
+ * ---------------------------------------------------------------------- */
+int gsort_segmented_bitonic(uint32_t *d_keys, int64_t num_segments,
+                            int segment_len, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Device-side status: synchronises `stream`, then returns GSORT_OK or the
+ * error a kernel recorded in this workspace during the last call that used
+ * it (GSORT_ETIMEOUT), or GSORT_ECUDA if the stream reports an error.
+ * ---------------------------------------------------------------------- */
+int gsort_check(const void *d_ws, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Extended calls: the same operations with options for tracing, tuning and
+ * testing.  A NULL options pointer means the defaults.
+ * ---------------------------------------------------------------------- */
+typedef struct gsort_options {
+    /* Polls of one look-back wait before the kernel records GSORT_ETIMEOUT
+     * and returns (0 = default, about a second of back-off). */
+    uint32_t spin_limit;
+    /* Testing only: the tile with this id never publishes its counts, so
+     * waits behind it run out.  -1 = none. */
+    int64_t stall_tile;
+    /* Optional array of cudaEvent_t handles recorded on `stream` around the
+     * launches: radix: [0] start, [1] after init, [2] after histogram,
+     * [3 + p] after digit pass p; compaction: [0] start, [1] after init,
+     * [2] after the scan/scatter kernel, [3] after the zero fill.  Extra
+     * entries are left alone; missing ones are skipped. */
+    void **events;
+    int num_events;
+    /* Launch configuration of the digit passes (0 = default; see
+     * gsort_radix_variant_name()). */
+    int variant;
+} gsort_options;
+
+int gsort_radix_pairs_ex(const void *d_keys_in, void *d_keys_out,
+                         const uint32_t *d_vals_in, uint32_t *d_vals_out, int64_t n,
+                         int kind, int begin_bit, int end_bit,
+                         void *d_ws, size_t ws_bytes, cudaStream_t stream,
+                         const gsort_options *options);
+
+int gsort_compact_positive_ex(const float *d_in, float *d_out, int64_t n,
+                              int64_t *d_num_kept, void *d_ws, size_t ws_bytes,
+                              cudaStream_t stream, const gsort_options *options);
+
+/* Number of digit-pass launch configurations, and the name of one
+ * ("warps x items per thread, ranking method"); NULL if out of range. */
+int gsort_radix_num_variants(void);
+const char *gsort_radix_variant_name(int variant);
+
+/* Kernel launches one call makes (for launch accounting):
+ * radix: 2 + passes (+1 copy-back when sorting in place with an odd pass
+ * count); compaction: 3; segmented: 1 (0 when there is nothing to do). */
+int gsort_radix_launch_count(int64_t n, int begin_bit, int end_bit, int in_place);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GSORT_H */

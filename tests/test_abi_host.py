@@ -1,0 +1,139 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every symbol include/gsort.h declares, sizes workspaces as documented, and
+rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "gsort.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bitonic_networks_gb300 import _lib
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(gsort_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_four_calls():
+    names = declared_functions()
+    for n in ("gsort_radix_keys", "gsort_radix_pairs", "gsort_compact_positive",
+              "gsort_segmented_bitonic"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from bitonic_networks_gb300 import _lib
+    names = declared_functions()
+    assert names, "no declarations parsed"
+    for name in names:
+        assert hasattr(lib, name), f"libgsort.so does not export {name}"
+        assert name in _lib.SIGNATURES, f"binding lacks a signature for {name}"
+
+
+def test_status_strings_and_version(lib):
+    assert lib.gsort_status_string(0) == b"GSORT_OK"
+    for code in range(-6, 0):
+        assert lib.gsort_status_string(code).startswith(b"GSORT_E")
+    assert lib.gsort_version() >= 100
+    assert lib.gsort_radix_num_variants() >= 1
+    for v in range(lib.gsort_radix_num_variants()):
+        assert lib.gsort_radix_variant_name(v)
+    assert lib.gsort_radix_variant_name(99) is None
+
+
+def test_workspace_sizes(lib):
+    HDR = 8192
+    for n in (1, 4095, 4096, 4097, 65536, 1 << 24, (1 << 30) - 1):
+        tiles = (n + 4095) // 4096
+        region = -(-tiles * 1024 // 256) * 256
+        keys = -(-n * 4 // 256) * 256
+        assert lib.gsort_radix_workspace_bytes(n, 0) == HDR + 2 * region + keys
+        assert lib.gsort_radix_workspace_bytes(n, 1) == HDR + 2 * region + 2 * keys
+        ctiles = (n + 8191) // 8192
+        assert lib.gsort_compact_workspace_bytes(n) == HDR + -(-ctiles * 4 // 256) * 256
+    assert lib.gsort_radix_workspace_bytes(-1, 0) == 0
+    assert lib.gsort_radix_workspace_bytes(1 << 30, 0) == 0
+    assert lib.gsort_compact_workspace_bytes(1 << 30) == 0
+
+
+def test_launch_count(lib):
+    assert lib.gsort_radix_launch_count(100, 0, 32, 0) == 6
+    assert lib.gsort_radix_launch_count(100, 0, 8, 0) == 3
+    assert lib.gsort_radix_launch_count(100, 0, 24, 1) == 6
+    assert lib.gsort_radix_launch_count(0, 0, 32, 0) == 0
+    assert lib.gsort_radix_launch_count(100, 5, 5, 0) == 0
+
+
+# Fake device addresses: validation rejects these calls before any CUDA call.
+A = 0x10000000
+B = 0x20000000
+W = 0x40000000
+EINVAL, EALIGN, EWS, ETOOBIG = -1, -2, -3, -4
+
+
+def test_radix_argument_errors(lib):
+    big = 1 << 40
+    f = lib.gsort_radix_pairs
+    assert f(A, B, None, None, 0, 0, 0, 32, None, 0, None) == 0          # n == 0: no-op
+    assert f(A, B, None, None, -1, 0, 0, 32, W, big, None) == EINVAL
+    assert f(A, B, None, None, 1 << 30, 0, 0, 32, W, big, None) == ETOOBIG
+    assert f(A, B, None, None, 10, 2, 0, 32, W, big, None) == EINVAL      # bad kind
+    assert f(A, B, None, None, 10, 0, 5, 4, W, big, None) == EINVAL       # begin > end
+    assert f(A, B, None, None, 10, 0, 0, 33, W, big, None) == EINVAL
+    assert f(A, B, None, None, 10, 0, -1, 8, W, big, None) == EINVAL
+    assert f(None, B, None, None, 10, 0, 0, 32, W, big, None) == EINVAL
+    assert f(A, B, A + 0x1000, None, 10, 0, 0, 32, W, big, None) == EINVAL   # values half given
+    assert f(A + 2, B, None, None, 10, 0, 0, 32, W, big, None) == EALIGN
+    assert f(A, B + 1, None, None, 10, 0, 0, 32, W, big, None) == EALIGN
+    assert f(A, A + 4, None, None, 10, 0, 0, 32, W, big, None) == EINVAL     # partial overlap
+    assert f(A, B, None, None, 10, 0, 0, 32, None, big, None) == EWS
+    assert f(A, B, None, None, 10, 0, 0, 32, W, 100, None) == EWS
+    assert f(A, B, None, None, 10, 0, 0, 32, W + 16, big, None) == EALIGN     # ws not 256-aligned
+    assert f(A, B, None, None, 10, 0, 0, 32, A, big, None) == EINVAL          # ws overlaps keys
+    # keys and values must not share memory
+    assert f(A, B, A + 0x100000, B, 10, 0, 0, 32, W, big, None) == EINVAL
+    assert lib.gsort_radix_keys(A, B, -5, 0, W, big, None) == EINVAL
+    assert lib.gsort_radix_keys(A, B, 10, 7, W, big, None) == EINVAL
+    opt = __import__("bitonic_networks_gb300._lib", fromlist=["Options"]).Options(0, -1, None, 0, 999)
+    assert lib.gsort_radix_pairs_ex(A, B, None, None, 10, 0, 0, 32, W, big, None,
+                                    ctypes.byref(opt)) == EINVAL            # no such variant
+
+
+def test_compaction_and_segment_argument_errors(lib):
+    big = 1 << 40
+    f = lib.gsort_compact_positive
+    assert f(A, B, -1, None, W, big, None) == EINVAL
+    assert f(A, B, 1 << 30, None, W, big, None) == ETOOBIG
+    assert f(None, B, 10, None, W, big, None) == EINVAL
+    assert f(A + 1, B, 10, None, W, big, None) == EALIGN
+    assert f(A, A + 8, 10, None, W, big, None) == EINVAL                      # overlap
+    assert f(A, B, 10, W + 4, W + 0x1000, big, None) == EALIGN                # num_kept alignment
+    assert f(A, B, 10, None, None, big, None) == EWS
+    assert f(A, B, 10, None, W, 16, None) == EWS
+    g = lib.gsort_segmented_bitonic
+    assert g(A, 10, 0, None) == EINVAL
+    assert g(A, 10, 1025, None) == EINVAL
+    assert g(A, -1, 16, None) == EINVAL
+    assert g(A, 1 << 31, 16, None) == ETOOBIG
+    assert g(A, 0, 16, None) == 0
+    assert g(A, 10, 1, None) == 0
+    assert g(None, 10, 16, None) == EINVAL
+    assert g(A + 2, 10, 16, None) == EALIGN
+    h = lib.gsort_digit_histograms
+    assert h(A, 10, 0, 0, 32, None, None) == EINVAL
+    assert h(A, 10, 0, 0, 40, B, None) == EINVAL
+    assert h(A, 10, 0, 0, 32, B + 2, None) == EALIGN
+    assert h(A, 1000, 0, 0, 32, A + 64, None) == EINVAL                       # output inside keys
+    assert h(A, 10, 0, 7, 7, B, None) == 0
+    assert lib.gsort_check(None, None) == EINVAL
