@@ -236,6 +236,10 @@ def main():
         raise RuntimeError("device-side error during warm-up")
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    for evs in events:          # torch creates the CUDA event on its first record
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
     clocks = Clocks(device.index)
     barrier()
     clocks.start()

@@ -79,6 +79,9 @@ def compact_workspace_bytes(n: int) -> int:
 def _events_arg(events):
     if not events:
         return None, 0
+    for e in events:            # torch creates the CUDA event on its first record
+        if e.cuda_event == 0:
+            e.record()
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     return arr, len(events)
 

@@ -1,0 +1,72 @@
+"""Runs one library call on a seeded input, for profilers (ncu).
+
+    python -m bitonic_networks_gb300.profile_cases OP [--n-log2 K] [--warmup W]
+           [--reps R] [--variant V]
+
+OP: keys (uint32 keys, 32 bits), pairs (uint32 key/index pairs), fpairs
+(float keys with index values), compact (compaction input), segments (1024-key
+segments, n/1024 of them), hist (the digit-histogram step alone).
+Each call is followed by a device-status check; the process exits non-zero on
+any error, so a profiler only ever runs a command that finished cleanly.
+"""
+from __future__ import annotations
+
+import argparse
+import sys
+
+import numpy as np
+import torch
+
+from . import _lib, gsort, synth
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("op", choices=["keys", "pairs", "fpairs", "compact", "segments", "hist"])
+    ap.add_argument("--n-log2", type=int, default=26)
+    ap.add_argument("--warmup", type=int, default=1)
+    ap.add_argument("--reps", type=int, default=1)
+    ap.add_argument("--variant", type=int, default=0)
+    a = ap.parse_args(argv)
+    n = 1 << a.n_log2
+    dev = torch.device("cuda", 0)
+
+    def up(x: np.ndarray) -> torch.Tensor:
+        x = np.ascontiguousarray(x)
+        return torch.from_numpy(x.view(np.int32) if x.dtype == np.uint32 else x).to(dev)
+
+    if a.op in ("keys", "hist"):
+        x = up(synth.uniform_keys(n, 1))
+    elif a.op == "pairs":
+        x, v = up(synth.uniform_keys(n, 2)), up(synth.index_values(n))
+    elif a.op == "fpairs":
+        x, v = up(synth.normal_f32_with_specials(n, 3)), up(synth.index_values(n))
+    elif a.op == "compact":
+        x = up(synth.compaction_input(n, 4))
+    else:
+        seg = up(synth.segments(n // 1024, 1024, 5))
+        x = seg.clone()
+
+    def once():
+        if a.op == "keys":
+            gsort.sort_pairs(x, None, variant=a.variant)
+        elif a.op in ("pairs", "fpairs"):
+            gsort.sort_pairs(x, v, variant=a.variant)
+        elif a.op == "compact":
+            gsort.compact_positive(x)
+        elif a.op == "hist":
+            gsort.digit_histograms(x)
+        else:
+            x.copy_(seg)
+            gsort.segmented_sort_(x.view(-1, 1024))
+
+    for _ in range(a.warmup + a.reps):
+        once()
+    torch.cuda.synchronize()
+    print(f"{a.op}: n=2^{a.n_log2} warmup={a.warmup} reps={a.reps} variant={a.variant} "
+          f"({_lib.load().gsort_radix_variant_name(a.variant).decode()}) ok")
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
