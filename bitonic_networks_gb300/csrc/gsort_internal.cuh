@@ -23,10 +23,11 @@ constexpr size_t kHdrBytes = 8192;    // header size, keeps what follows 256-byt
 constexpr size_t kWsAlign = 256;
 
 // ------------------------------------------------------------ look-back words
-// One 32-bit word per (tile[, digit]): 2 flag bits and a 30-bit count.
-// 0 = nothing published yet; AGG = the tile's own count; PREFIX = the count
-// over this tile and every earlier tile ([CUDA3] decoupled look-back: three
-// states per block).  The 30-bit field is why n <= 2^30 - 1.
+// Three states per tile ([CUDA3] decoupled look-back): 0 = nothing published
+// yet; AGG = the tile's own count is published; PREFIX = the count over this
+// tile and every earlier tile is published.  The state sits in the top two
+// bits of a 32-bit word whose low 30 bits hold the count (hence n <= 2^30 - 1):
+// one word per tile (compaction) or per tile and digit (radix sort).
 constexpr uint32_t kFlagAgg = 1u << 30;
 constexpr uint32_t kFlagPrefix = 2u << 30;
 constexpr uint32_t kValueMask = (1u << 30) - 1;
@@ -47,6 +48,19 @@ __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p) {
 
 __device__ __forceinline__ void st_relaxed(uint32_t *p, uint32_t v) {
     asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Atomic add with release semantics: every write that precedes it (in this
+// thread, or in threads ordered before it by a barrier) is visible to a
+// thread that observes the new value with an acquire load.
+__device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
@@ -89,6 +103,53 @@ __device__ __forceinline__ void backoff(uint32_t &ns) {
     if (ns < 1024) ns <<= 1;
 }
 
+// ------------------------------------------- mbarrier + TMA bulk copies
+// One-dimensional bulk copies global -> shared through the tensor memory
+// accelerator, completed on an mbarrier (transaction-count based).  Both
+// addresses and the size must be multiples of 16 bytes.
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Waits for phase `parity` of the barrier, at most `limit` polls.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src_gmem, uint32_t bytes,
+                                          uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_addr(dst_smem)), "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
 // -------------------------------------------------------- host-side helpers
 struct DeviceInfo {
     int device;
@@ -119,8 +180,8 @@ struct RadixLaunch {
 
 // Layout of the radix workspace after the header.
 struct RadixLayout {
-    uint32_t tiles_max;   // look-back rows per region
-    size_t look_a, look_b;
+    uint32_t tiles_max;   // tiles of the smallest tile size any variant uses
+    size_t look_a, look_b;  // [tiles_max][256] look-back words, alternating between passes
     size_t tmp_keys, tmp_vals;
     size_t total;
 };

@@ -5,7 +5,7 @@
 //   histogram  one read of the keys builds the 256-bin histogram of every
 //              digit pass ([CUDA3] "processing several bits at once", kernel 1;
 //              [PMPP10] 10.3 histogram step) and clears the first pass's
-//              look-back region
+//              look-back words
 //   P x pass   single-pass digit scatter ([CUDA3] kernel 3): each tile ranks
 //              its keys stably per digit with a warp multisplit, publishes its
 //              per-digit counts, looks back over earlier tiles' counts
@@ -19,10 +19,12 @@
 //              buffering).  Values move with their keys ([PMPP10] 10.6).
 //
 // Differences from the pages' kernels: the in-tile rank comes from a warp
-// multisplit (peer mask of equal digits + popcount below the lane, one
-// shared counter per warp and digit) instead of eight block-wide 1-bit splits;
-// look-back regions are cleared one row per tile by the previous kernel
-// instead of a memset per pass; every wait is bounded.
+// multisplit (peer mask of equal digits + popcount below the lane) instead of
+// eight block-wide 1-bit splits; a tile counts its digits first (cheap shared
+// atomics) and publishes the counts before ranking, so its look-back overlaps
+// other warps' ranking, and the per-warp counters then hand out tile slots
+// directly; look-back words are cleared one row per tile by the previous
+// kernel instead of a memset per pass; every wait is bounded.
 #include <algorithm>
 
 #include "gsort_internal.cuh"
@@ -38,37 +40,54 @@ __global__ void k_zero_words(uint32_t *p, uint32_t nwords) {
 }
 
 // -------------------------------------------------------------- histogram
-constexpr int kHistThreads = 256;
-constexpr int kHistParts = 4;     // sub-histograms by lane, spreading same-digit atomics
+// Every lane owns a private column of counters: counter (pass, digit, lane)
+// sits at word ((pass*256 + digit) * 32 + lane), i.e. always in bank `lane`,
+// so the shared-memory atomics of a warp never conflict, whatever the keys
+// (equal keys included).  One 1024-thread CTA per SM, 128 KiB of counters;
+// the columns are summed once per CTA and added to the global histogram.
+constexpr int kHistThreads = 1024;
 constexpr int kHistUnroll = 4;    // 16-byte loads in flight per thread
 
-template <bool XF>
-__device__ __forceinline__ void hist_count(uint32_t *s_h, uint32_t k, uint32_t begin_bit,
-                                           int passes, uint32_t last_mask, uint32_t part) {
+__host__ __device__ constexpr size_t hist_smem_bytes(int passes) {
+    return static_cast<size_t>(passes) * 256 * 32 * sizeof(uint32_t);
+}
+
+// Digit p of key k.  BYTE: the digits are whole bytes of the key (begin_bit a
+// multiple of 8, full 8-bit masks) and are extracted with one byte permute.
+template <bool BYTE>
+__device__ __forceinline__ uint32_t digit_at(uint32_t k, uint32_t shift, uint32_t mask) {
+    if constexpr (BYTE) return __byte_perm(k, 0u, 0x4440u | (shift >> 3));
+    else return (k >> shift) & mask;
+}
+
+template <bool XF, bool BYTE>
+__device__ __forceinline__ void hist_count(uint32_t *col, uint32_t k, uint32_t begin_bit,
+                                           int passes, uint32_t last_mask) {
     if (XF) k = float_key_in(k);
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
         if (p < passes) {
-            const uint32_t d = (k >> (begin_bit + 8 * p)) & (p == passes - 1 ? last_mask : 0xFFu);
-            atomicAdd(&s_h[(p * 256 + d) * kHistParts + part], 1u);
+            const uint32_t d = digit_at<BYTE>(k, begin_bit + 8 * p, p == passes - 1 ? last_mask : 0xFFu);
+            atomicAdd(&col[(p * 256 + d) * 32], 1u);
         }
     }
 }
 
-template <bool XF>
-__global__ void __launch_bounds__(kHistThreads)
+template <bool XF, bool BYTE>
+__global__ void __launch_bounds__(kHistThreads, 1)
 k_digit_hist(const uint32_t *__restrict__ keys, uint32_t n, uint32_t begin_bit, int passes,
              uint32_t last_mask, uint32_t *__restrict__ hist, uint4 *__restrict__ clear,
              uint32_t clear_vec4) {
-    __shared__ uint32_t s_h[4 * 256 * kHistParts];
+    extern __shared__ uint32_t s_h[];
     const uint32_t tid = threadIdx.x;
-    for (uint32_t i = tid; i < 4 * 256 * kHistParts; i += kHistThreads) s_h[i] = 0;
+    const uint32_t words = static_cast<uint32_t>(passes) * 256 * 32;
+    for (uint32_t i = tid; i < words; i += kHistThreads) s_h[i] = 0;
     const uint32_t gtid = blockIdx.x * kHistThreads + tid;
     const uint32_t gstride = gridDim.x * kHistThreads;
     for (uint32_t i = gtid; i < clear_vec4; i += gstride) clear[i] = make_uint4(0, 0, 0, 0);
     __syncthreads();
 
-    const uint32_t part = tid & (kHistParts - 1);
+    uint32_t *col = s_h + (tid & 31);
     // elements before the first 16-byte boundary, the vector body, the tail
     uint32_t head = static_cast<uint32_t>(((16 - (reinterpret_cast<uintptr_t>(keys) & 15)) & 15) >> 2);
     head = min(head, n);
@@ -84,22 +103,24 @@ k_digit_hist(const uint32_t *__restrict__ keys, uint32_t n, uint32_t begin_bit, 
 #pragma unroll
         for (int u = 0; u < kHistUnroll; ++u) {
             if (v + u * gstride < nvec) {
-                hist_count<XF>(s_h, q[u].x, begin_bit, passes, last_mask, part);
-                hist_count<XF>(s_h, q[u].y, begin_bit, passes, last_mask, part);
-                hist_count<XF>(s_h, q[u].z, begin_bit, passes, last_mask, part);
-                hist_count<XF>(s_h, q[u].w, begin_bit, passes, last_mask, part);
+                hist_count<XF, BYTE>(col, q[u].x, begin_bit, passes, last_mask);
+                hist_count<XF, BYTE>(col, q[u].y, begin_bit, passes, last_mask);
+                hist_count<XF, BYTE>(col, q[u].z, begin_bit, passes, last_mask);
+                hist_count<XF, BYTE>(col, q[u].w, begin_bit, passes, last_mask);
             }
         }
     }
     const uint32_t tail0 = head + nvec * 4;
-    if (gtid < head) hist_count<XF>(s_h, keys[gtid], begin_bit, passes, last_mask, part);
-    if (gtid < n - tail0) hist_count<XF>(s_h, keys[tail0 + gtid], begin_bit, passes, last_mask, part);
+    if (gtid < head) hist_count<XF, BYTE>(col, keys[gtid], begin_bit, passes, last_mask);
+    if (gtid < n - tail0) hist_count<XF, BYTE>(col, keys[tail0 + gtid], begin_bit, passes, last_mask);
     __syncthreads();
 
+    // sum each (pass, digit) row over the 32 lane columns; the rotated start
+    // keeps the 32 threads of a warp on 32 different banks
     for (uint32_t i = tid; i < static_cast<uint32_t>(passes) * 256; i += kHistThreads) {
         uint32_t s = 0;
-#pragma unroll
-        for (int q = 0; q < kHistParts; ++q) s += s_h[i * kHistParts + q];
+#pragma unroll 8
+        for (uint32_t j = 0; j < 32; ++j) s += s_h[i * 32 + ((j + i) & 31)];
         if (s) atomicAdd(&hist[i], s);
     }
 }
@@ -114,8 +135,8 @@ struct PassArgs {
     uint32_t shift;         // digit = (key >> shift) & mask
     uint32_t mask;
     const uint32_t *hist;   // the 256 counts of this pass
-    uint32_t *look;         // [tiles][256] look-back words of this pass (cleared)
-    uint32_t *look_clear;   // next pass's region: row `tile` is cleared here; may be null
+    uint32_t *look;         // [tiles][256] look-back words of this pass (cleared): flag | count
+    uint32_t *look_clear;   // next pass's words: row `tile` is cleared here; may be null
     uint32_t *tile_counter;
     uint32_t *status;
     uint32_t *abort_flag;
@@ -123,40 +144,111 @@ struct PassArgs {
     uint32_t stall_tile;
 };
 
-// Mask of the lanes whose digit equals this lane's digit.  BITS = digit
-// width considered (8, or 9 when padding items carry the pseudo-digit 256).
-template <int BITS, bool HW>
-__device__ __forceinline__ uint32_t match_digit(uint32_t d) {
-    if constexpr (HW) {
+// ------------------------------------------------------- warp multisplit
+// Ranking methods for the mask of lanes whose digit equals this lane's:
+//   kMatchTable  the eight ballots (bit planes of the warp's digits) are turned
+//                into two lane-distributed tables: lane l holds the mask of
+//                lanes whose low five digit bits equal l, and the mask of lanes
+//                whose top three bits equal l & 7 (built with per-lane
+//                constants, no per-key bit tests); a lane fetches its two
+//                entries with two shuffles and ANDs them.
+//   kMatchSelect each lane selects, per bit, the ballot or its complement.
+//   kMatchAny    the hardware match.any instruction.
+constexpr int kMatchTable = 0, kMatchSelect = 1, kMatchAny = 2;
+
+struct LaneConsts {
+    uint32_t inv[5];   // ~0 where bit b of the lane id is 0, else 0
+};
+
+__device__ __forceinline__ LaneConsts lane_consts(uint32_t lane) {
+    LaneConsts c;
+#pragma unroll
+    for (int b = 0; b < 5; ++b) c.inv[b] = ((lane >> b) & 1u) ? 0u : kFullMask;
+    return c;
+}
+
+template <int MATCH>
+__device__ __forceinline__ uint32_t digit_peers(uint32_t d, const LaneConsts &c) {
+    if constexpr (MATCH == kMatchAny) {
         return __match_any_sync(kFullMask, d);
-    } else {
+    } else if constexpr (MATCH == kMatchSelect) {
         uint32_t peers = kFullMask;
 #pragma unroll
-        for (int b = 0; b < BITS; ++b) {
+        for (int b = 0; b < 8; ++b) {
             const bool bit = (d >> b) & 1u;
             const uint32_t m = __ballot_sync(kFullMask, bit);
             peers &= bit ? m : ~m;
         }
         return peers;
+    } else {
+        uint32_t m[8];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) m[b] = __ballot_sync(kFullMask, (d >> b) & 1u);
+        const uint32_t lo = (m[0] ^ c.inv[0]) & (m[1] ^ c.inv[1]) & (m[2] ^ c.inv[2]) &
+                            (m[3] ^ c.inv[3]) & (m[4] ^ c.inv[4]);
+        const uint32_t hi = (m[5] ^ c.inv[0]) & (m[6] ^ c.inv[1]) & (m[7] ^ c.inv[2]);
+        return __shfl_sync(kFullMask, lo, d & 31u) & __shfl_sync(kFullMask, hi, d >> 5);
     }
 }
 
-constexpr int kRow = 257;   // per-warp digit counters, slot 256 = padding items
+constexpr int kRow = 256;   // per-warp digit counters
 
 template <int WARPS, int IPT, bool PAIRS>
 constexpr size_t pass_smem_words() {
+    // keys [+ values] of the tile, per-warp counters, 256 digit offsets, 32 misc words
     return static_cast<size_t>(WARPS * 32 * IPT) * (PAIRS ? 2 : 1) + WARPS * kRow + 256 + 32;
 }
 
-template <int WARPS, int IPT, bool HWM, bool PAIRS, bool XIN, bool XOUT, bool FULL>
+constexpr int kLookWindow = 8;   // predecessor tiles read per look-back round
+
+// Exclusive prefix of digit d over all tiles before `tile`.  Each word holds a
+// flag (AGG: the tile's count; PREFIX: the count over tiles 0..t) and a
+// 30-bit count, so one round trip reads kLookWindow predecessors at once; the
+// nearest PREFIX word ends the walk and the AGG words before it are summed.
+// Returns false if a wait gave up.
+__device__ __forceinline__ bool look_back(const PassArgs &a, uint32_t tile, uint32_t d,
+                                          uint32_t &excl) {
+    excl = 0;
+    int32_t t = static_cast<int32_t>(tile) - 1;
+    uint32_t polls = 0, ns = 32;
+    while (true) {
+        uint32_t w[kLookWindow];
+#pragma unroll
+        for (int i = 0; i < kLookWindow; ++i)
+            w[i] = (t - i >= 0) ? ld_relaxed(a.look + static_cast<uint32_t>(t - i) * 256 + d)
+                                : kFlagPrefix;   // before tile 0: an empty prefix
+        // sum words up to and including the nearest PREFIX; any empty word
+        // before it means a predecessor has not published yet
+        uint32_t sum = 0;
+        bool done = false, pending = false;
+#pragma unroll
+        for (int i = 0; i < kLookWindow; ++i) {
+            if (!done) {
+                pending |= (w[i] & ~kValueMask) == 0;
+                sum += w[i] & kValueMask;
+                done = (w[i] & kFlagPrefix) != 0;
+            }
+        }
+        if (pending) {
+            if (++polls >= a.spin_limit || ld_relaxed(a.abort_flag)) return false;
+            backoff(ns);
+            continue;
+        }
+        excl += sum;
+        if (done) return true;
+        t -= kLookWindow;
+    }
+}
+
+template <int WARPS, int IPT, int MATCH, bool BYTE, bool PAIRS, bool XIN, bool XOUT, bool FULL>
 __device__ __forceinline__ void pass_tile(const PassArgs &a, uint32_t *smem, uint32_t tile) {
     constexpr int T = WARPS * 32;
     constexpr int TILE = T * IPT;
     uint32_t *s_keys = smem;
     uint32_t *s_vals = smem + TILE;
-    uint32_t *s_cnt = smem + TILE * (PAIRS ? 2 : 1);
-    uint32_t *s_goff = s_cnt + WARPS * kRow;
-    uint32_t *s_misc = s_goff + 256;
+    uint32_t *s_cnt = smem + TILE * (PAIRS ? 2 : 1);   // [WARPS][256] counts, then next free slots
+    uint32_t *s_goff = s_cnt + WARPS * kRow;            // [256] global index - tile slot
+    uint32_t *s_misc = s_goff + 256;                    // [32]
 
     const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t tile_base = tile * TILE;
@@ -173,30 +265,6 @@ __device__ __forceinline__ void pass_tile(const PassArgs &a, uint32_t *smem, uin
         key[k] = (FULL || i < tile_n) ? a.src_k[tile_base + i] : 0u;
         if (XIN) key[k] = float_key_in(key[k]);
     }
-
-    // ---- warp multisplit: stable rank among this warp's keys of each digit
-    uint32_t pos[IPT];
-    {
-        uint32_t *wc = s_cnt + warp * kRow;
-        const uint32_t ltm = lanemask_lt();
-#pragma unroll
-        for (int k = 0; k < IPT; ++k) {
-            uint32_t d = (key[k] >> a.shift) & a.mask;
-            uint32_t peers;
-            if (FULL) {
-                peers = match_digit<8, HWM>(d);
-            } else {
-                if (item0 + k * 32 >= tile_n) d = 256;
-                peers = match_digit<9, HWM>(d);
-            }
-            const int leader = 31 - __clz(peers);
-            uint32_t base = 0;
-            if (lane == static_cast<uint32_t>(leader)) base = atomicAdd(&wc[d], static_cast<uint32_t>(__popc(peers)));
-            base = __shfl_sync(kFullMask, base, leader);
-            pos[k] = base + __popc(peers & ltm);
-        }
-    }
-
     uint32_t val[PAIRS ? IPT : 1];
     if (PAIRS) {
 #pragma unroll
@@ -205,20 +273,28 @@ __device__ __forceinline__ void pass_tile(const PassArgs &a, uint32_t *smem, uin
             val[k] = (FULL || i < tile_n) ? a.src_v[tile_base + i] : 0u;
         }
     }
+
+    // ---- early counts: this warp's keys per digit (order does not matter here)
+    {
+        uint32_t *wc = s_cnt + warp * kRow;
+#pragma unroll
+        for (int k = 0; k < IPT; ++k)
+            if (FULL || item0 + k * 32 < tile_n) atomicAdd(&wc[digit_at<BYTE>(key[k], a.shift, a.mask)], 1u);
+    }
     __syncthreads();
 
-    // ---- tile counts per digit; publish them; scans over the 256 digits
-    uint32_t cnt = 0, bin = 0, tile_excl = 0, bin_excl = 0;
+    // ---- tile counts per digit, published at once; scans over the 256 digits
+    uint32_t cnt = 0, tile_excl = 0, bin_excl = 0;
     if (tid < 256) {
 #pragma unroll
         for (int w = 0; w < WARPS; ++w) {
-            const uint32_t c = s_cnt[w * kRow + tid];
+            const uint32_t cw = s_cnt[w * kRow + tid];
             s_cnt[w * kRow + tid] = cnt;   // exclusive over warps
-            cnt += c;
+            cnt += cw;
         }
         if (tile != a.stall_tile)
             st_relaxed(a.look + tile * 256 + tid, (tile == 0 ? kFlagPrefix : kFlagAgg) | cnt);
-        bin = a.hist[tid];
+        const uint32_t bin = a.hist[tid];
         const uint32_t ic = warp_inclusive_scan(cnt, lane);
         const uint32_t ib = warp_inclusive_scan(bin, lane);
         if (lane == 31) {
@@ -228,56 +304,62 @@ __device__ __forceinline__ void pass_tile(const PassArgs &a, uint32_t *smem, uin
         tile_excl = ic - cnt;
         bin_excl = ib - bin;
     }
+    if (a.look_clear != nullptr)
+        for (uint32_t i = tid; i < 256; i += T) a.look_clear[tile * 256 + i] = 0;
     __syncthreads();
-
-    // ---- decoupled look-back, one digit per thread
     if (tid < 256) {
         for (uint32_t w = 0; w < warp; ++w) {
             tile_excl += s_misc[4 + w];
             bin_excl += s_misc[12 + w];
         }
+        // s_cnt[w][d]: tile slot where warp w's first key of digit d goes
+#pragma unroll
+        for (int w = 0; w < WARPS; ++w) s_cnt[w * kRow + tid] += tile_excl;
+    }
+    __syncthreads();
+
+    // ---- decoupled look-back, one digit per thread of the first 8 warps
+    // (the other warps rank meanwhile); then publish this tile's prefixes
+    if (tid < 256) {
         uint32_t excl = 0;
         bool ok = true;
         if (tile > 0 && tile != a.stall_tile) {
-            int32_t t = static_cast<int32_t>(tile) - 1;
-            uint32_t polls = 0, ns = 32;
-            while (true) {
-                if (t < 0) { ok = false; break; }   // tile 0 always publishes a prefix
-                const uint32_t s = ld_relaxed(a.look + static_cast<uint32_t>(t) * 256 + tid);
-                if ((s & ~kValueMask) == 0) {
-                    if (++polls >= a.spin_limit || ld_relaxed(a.abort_flag)) { ok = false; break; }
-                    backoff(ns);
-                    continue;
-                }
-                excl += s & kValueMask;
-                if (s & kFlagPrefix) break;
-                --t;
-            }
+            ok = look_back(a, tile, tid, excl);
             if (ok) st_relaxed(a.look + tile * 256 + tid, kFlagPrefix | (excl + cnt));
         }
         if (!ok) {
             s_misc[2] = 1;
             record_error(a.status, a.abort_flag, GSORT_ETIMEOUT);
         }
-        // global index = bin start + earlier tiles + (tile-local slot - tile start of digit)
+        // global index of tile slot i holding digit d: s_goff[d] + i
         s_goff[tid] = bin_excl + excl - tile_excl;
-#pragma unroll
-        for (int w = 0; w < WARPS; ++w) s_cnt[w * kRow + tid] += tile_excl;
     }
-    __syncthreads();
-    if (s_misc[2] || tile == a.stall_tile) return;
 
-    // ---- reorder the tile by digit in shared memory
+    // ---- warp multisplit: stable slot of each key in the tile-sorted order
+    {
+        uint32_t *wc = s_cnt + warp * kRow;
+        const uint32_t ltm = lanemask_lt();
+        const LaneConsts c = lane_consts(lane);
 #pragma unroll
-    for (int k = 0; k < IPT; ++k) {
-        if (FULL || item0 + k * 32 < tile_n) {
-            const uint32_t d = (key[k] >> a.shift) & a.mask;
-            const uint32_t p = pos[k] + s_cnt[warp * kRow + d];
-            s_keys[p] = key[k];
-            if (PAIRS) s_vals[p] = val[k];
+        for (int k = 0; k < IPT; ++k) {
+            const bool valid = FULL || item0 + k * 32 < tile_n;
+            const uint32_t d = valid ? digit_at<BYTE>(key[k], a.shift, a.mask) : 0u;
+            uint32_t peers = digit_peers<MATCH>(d, c);
+            if (!FULL) peers &= __ballot_sync(kFullMask, valid);
+            const int leader = 31 - __clz(peers);
+            uint32_t base = 0;
+            if (valid && lane == static_cast<uint32_t>(leader))
+                base = atomicAdd(&wc[d], static_cast<uint32_t>(__popc(peers)));
+            base = __shfl_sync(kFullMask, base, leader & 31);
+            if (valid) {
+                const uint32_t slot = base + __popc(peers & ltm);
+                s_keys[slot] = key[k];
+                if (PAIRS) s_vals[slot] = val[k];
+            }
         }
     }
     __syncthreads();
+    if (s_misc[2] || tile == a.stall_tile) return;
 
     // ---- contiguous runs per digit out to global memory
 #pragma unroll
@@ -285,7 +367,7 @@ __device__ __forceinline__ void pass_tile(const PassArgs &a, uint32_t *smem, uin
         const uint32_t i = k * T + tid;
         if (FULL || i < tile_n) {
             const uint32_t kk = s_keys[i];
-            const uint32_t g = s_goff[(kk >> a.shift) & a.mask] + i;
+            const uint32_t g = s_goff[digit_at<BYTE>(kk, a.shift, a.mask)] + i;
             if (g < a.n) {
                 a.dst_k[g] = XOUT ? float_key_out(kk) : kk;
                 if (PAIRS) a.dst_v[g] = s_vals[i];
@@ -294,7 +376,7 @@ __device__ __forceinline__ void pass_tile(const PassArgs &a, uint32_t *smem, uin
     }
 }
 
-template <int WARPS, int IPT, int MINB, bool HWM, bool PAIRS, bool XIN, bool XOUT>
+template <int WARPS, int IPT, int MINB, int MATCH, bool BYTE, bool PAIRS, bool XIN, bool XOUT>
 __global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass(const PassArgs a) {
     constexpr int TILE = WARPS * 32 * IPT;
     extern __shared__ uint32_t smem[];
@@ -310,22 +392,20 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass(const PassArgs 
     __syncthreads();
     const uint32_t tile = s_misc[0];
     if (s_misc[1]) return;   // an earlier wait gave up; the result is void anyway
-    if (a.look_clear != nullptr)
-        for (uint32_t i = tid; i < 256; i += WARPS * 32) a.look_clear[tile * 256 + i] = 0;
     if (a.n - tile * TILE >= static_cast<uint32_t>(TILE))
-        pass_tile<WARPS, IPT, HWM, PAIRS, XIN, XOUT, true>(a, smem, tile);
+        pass_tile<WARPS, IPT, MATCH, BYTE, PAIRS, XIN, XOUT, true>(a, smem, tile);
     else
-        pass_tile<WARPS, IPT, HWM, PAIRS, XIN, XOUT, false>(a, smem, tile);
+        pass_tile<WARPS, IPT, MATCH, BYTE, PAIRS, XIN, XOUT, false>(a, smem, tile);
 }
 
 // ------------------------------------------------------------ variants
-template <int WARPS, int IPT, int MINB, bool HWM>
+template <int WARPS, int IPT, int MINB, int MATCH>
 struct PassConfig {
     static constexpr uint32_t kTile = WARPS * 32 * IPT;
 
-    template <bool P, bool XI, bool XO>
+    template <bool B, bool P, bool XI, bool XO>
     static cudaError_t launch_one(const PassArgs &a, uint32_t tiles, cudaStream_t s) {
-        auto k = k_digit_pass<WARPS, IPT, MINB, HWM, P, XI, XO>;
+        auto k = k_digit_pass<WARPS, IPT, MINB, MATCH, B, P, XI, XO>;
         const size_t smem = pass_smem_words<WARPS, IPT, P>() * sizeof(uint32_t);
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
@@ -334,19 +414,27 @@ struct PassConfig {
         return cudaGetLastError();
     }
 
-    static cudaError_t launch(const PassArgs &a, bool pairs, bool xin, bool xout, uint32_t tiles,
-                              cudaStream_t s) {
+    template <bool B>
+    static cudaError_t launch_b(const PassArgs &a, bool pairs, bool xin, bool xout, uint32_t tiles,
+                                cudaStream_t s) {
         const int sel = (pairs ? 4 : 0) | (xin ? 2 : 0) | (xout ? 1 : 0);
         switch (sel) {
-            case 0: return launch_one<false, false, false>(a, tiles, s);
-            case 1: return launch_one<false, false, true>(a, tiles, s);
-            case 2: return launch_one<false, true, false>(a, tiles, s);
-            case 3: return launch_one<false, true, true>(a, tiles, s);
-            case 4: return launch_one<true, false, false>(a, tiles, s);
-            case 5: return launch_one<true, false, true>(a, tiles, s);
-            case 6: return launch_one<true, true, false>(a, tiles, s);
-            default: return launch_one<true, true, true>(a, tiles, s);
+            case 0: return launch_one<B, false, false, false>(a, tiles, s);
+            case 1: return launch_one<B, false, false, true>(a, tiles, s);
+            case 2: return launch_one<B, false, true, false>(a, tiles, s);
+            case 3: return launch_one<B, false, true, true>(a, tiles, s);
+            case 4: return launch_one<B, true, false, false>(a, tiles, s);
+            case 5: return launch_one<B, true, false, true>(a, tiles, s);
+            case 6: return launch_one<B, true, true, false>(a, tiles, s);
+            default: return launch_one<B, true, true, true>(a, tiles, s);
         }
+    }
+
+    static cudaError_t launch(const PassArgs &a, bool pairs, bool xin, bool xout, uint32_t tiles,
+                              cudaStream_t s) {
+        const bool byte = (a.shift % 8) == 0 && a.mask == 0xFFu;
+        return byte ? launch_b<true>(a, pairs, xin, xout, tiles, s)
+                    : launch_b<false>(a, pairs, xin, xout, tiles, s);
     }
 };
 
@@ -357,36 +445,33 @@ struct Variant {
 };
 
 const Variant kVariants[] = {
-    {"16 warps x 16 items, ballot multisplit", PassConfig<16, 16, 2, false>::kTile,
-     &PassConfig<16, 16, 2, false>::launch},
-    {"16 warps x 16 items, match.any multisplit", PassConfig<16, 16, 2, true>::kTile,
-     &PassConfig<16, 16, 2, true>::launch},
-    {"8 warps x 16 items, ballot multisplit", PassConfig<8, 16, 3, false>::kTile,
-     &PassConfig<8, 16, 3, false>::launch},
-    {"8 warps x 16 items, match.any multisplit", PassConfig<8, 16, 3, true>::kTile,
-     &PassConfig<8, 16, 3, true>::launch},
+    {"16 warps x 16 items, ballot tables", PassConfig<16, 16, 2, kMatchTable>::kTile,
+     &PassConfig<16, 16, 2, kMatchTable>::launch},
+    {"16 warps x 16 items, ballot select", PassConfig<16, 16, 2, kMatchSelect>::kTile,
+     &PassConfig<16, 16, 2, kMatchSelect>::launch},
+    {"16 warps x 16 items, match.any", PassConfig<16, 16, 2, kMatchAny>::kTile,
+     &PassConfig<16, 16, 2, kMatchAny>::launch},
+    {"8 warps x 16 items, ballot tables", PassConfig<8, 16, 3, kMatchTable>::kTile,
+     &PassConfig<8, 16, 3, kMatchTable>::launch},
 };
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
-
-uint32_t hist_grid(uint32_t n, int sm_count) {
-    const uint32_t vec = (n >> 2) + 1;
-    const uint32_t want = (vec + kHistThreads * kHistUnroll - 1) / (kHistThreads * kHistUnroll);
-    return std::max(1u, std::min(want, static_cast<uint32_t>(sm_count) * 8u));
-}
 
 cudaError_t launch_hist(const uint32_t *keys, uint32_t n, int kind, int begin_bit, int passes,
                         uint32_t last_mask, uint32_t *hist, uint32_t *clear, uint32_t clear_words,
                         cudaStream_t s, int sm_count) {
-    const uint32_t grid = std::max(hist_grid(n, sm_count),
-                                   std::min<uint32_t>(clear_words / 4 / kHistThreads + 1,
-                                                      static_cast<uint32_t>(sm_count) * 8u));
+    // one CTA per SM (fewer for small inputs: about 16 keys per thread at least)
+    const uint32_t want = (n + kHistThreads * 16 - 1) / (kHistThreads * 16);
+    const uint32_t grid = std::max(1u, std::min(want, static_cast<uint32_t>(sm_count)));
     uint4 *cl = reinterpret_cast<uint4 *>(clear);
-    if (kind == GSORT_KEY_F32)
-        k_digit_hist<true><<<grid, kHistThreads, 0, s>>>(keys, n, begin_bit, passes, last_mask,
-                                                         hist, cl, clear_words / 4);
-    else
-        k_digit_hist<false><<<grid, kHistThreads, 0, s>>>(keys, n, begin_bit, passes, last_mask,
-                                                          hist, cl, clear_words / 4);
+    const bool byte = (begin_bit % 8) == 0 && last_mask == 0xFFu;
+    auto k = (kind == GSORT_KEY_F32) ? (byte ? k_digit_hist<true, true> : k_digit_hist<true, false>)
+                                     : (byte ? k_digit_hist<false, true> : k_digit_hist<false, false>);
+    const size_t smem = hist_smem_bytes(passes);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(hist_smem_bytes(4)));
+    if (e != cudaSuccess) return e;
+    k<<<grid, kHistThreads, smem, s>>>(keys, n, begin_bit, passes, last_mask, hist, cl,
+                                       clear_words / 4);
     return cudaGetLastError();
 }
 
@@ -409,9 +494,9 @@ RadixLayout radix_layout(uint32_t n, bool with_values) {
     L.tiles_max = (n + kMinRadixTile - 1) / kMinRadixTile;
     size_t off = kHdrBytes;
     const size_t region = align_up(static_cast<size_t>(L.tiles_max) * 256 * sizeof(uint32_t), kWsAlign);
-    L.look_a = off;
+    L.look_a = off;   // [tiles_max][256] look-back words, passes 0, 2
     off += region;
-    L.look_b = off;
+    L.look_b = off;   // passes 1, 3
     off += region;
     L.tmp_keys = off;
     off += align_up(static_cast<size_t>(n) * sizeof(uint32_t), kWsAlign);
@@ -444,7 +529,8 @@ int launch_radix(const RadixLaunch &L) {
     record(L.events, L.num_events, 1, s);
 
     const uint32_t last_width = static_cast<uint32_t>(L.end_bit - L.begin_bit - 8 * (passes - 1));
-    const uint32_t last_mask = (last_width >= 32) ? 0xFFFFFFFFu : ((1u << last_width) - 1u);
+    const uint32_t last_mask = (1u << last_width) - 1u;
+    // the histogram kernel also clears the first pass's look-back words
     if (launch_hist(L.keys_in, L.n, L.kind, L.begin_bit, passes, last_mask, hist, look[0],
                     tiles * 256, s, L.sm_count) != cudaSuccess)
         return GSORT_ECUDA;

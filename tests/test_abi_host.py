@@ -54,12 +54,15 @@ def test_status_strings_and_version(lib):
 
 def test_workspace_sizes(lib):
     HDR = 8192
+
+    def up(x):
+        return -(-x // 256) * 256
     for n in (1, 4095, 4096, 4097, 65536, 1 << 24, (1 << 30) - 1):
         tiles = (n + 4095) // 4096
-        region = -(-tiles * 1024 // 256) * 256
-        keys = -(-n * 4 // 256) * 256
-        assert lib.gsort_radix_workspace_bytes(n, 0) == HDR + 2 * region + keys
-        assert lib.gsort_radix_workspace_bytes(n, 1) == HDR + 2 * region + 2 * keys
+        state = 2 * up(tiles * 1024)   # two alternating regions of look-back words
+        keys = up(n * 4)
+        assert lib.gsort_radix_workspace_bytes(n, 0) == HDR + state + keys
+        assert lib.gsort_radix_workspace_bytes(n, 1) == HDR + state + 2 * keys
         ctiles = (n + 8191) // 8192
         assert lib.gsort_compact_workspace_bytes(n) == HDR + -(-ctiles * 4 // 256) * 256
     assert lib.gsort_radix_workspace_bytes(-1, 0) == 0
