@@ -240,15 +240,21 @@ __device__ __forceinline__ bool look_back(const PassArgs &a, uint32_t tile, uint
     }
 }
 
+// One tile of a digit pass.  kin/vin point at the tile's first key/value (in
+// global memory, or in a shared staging buffer); the tile-sorted keys/values
+// go to s_keys/s_vals (which may be the staging buffers: every key is in
+// registers before the first write).  tab = the shared tables: per-warp digit
+// counters, digit offsets, misc words.  Returns false when the tile stops
+// (device error or the test stall), after a block barrier.
 template <int WARPS, int IPT, int MATCH, bool BYTE, bool PAIRS, bool XIN, bool XOUT, bool FULL>
-__device__ __forceinline__ void pass_tile(const PassArgs &a, uint32_t *smem, uint32_t tile) {
+__device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, uint32_t tile,
+                                          const uint32_t *kin, const uint32_t *vin,
+                                          uint32_t *s_keys, uint32_t *s_vals) {
     constexpr int T = WARPS * 32;
     constexpr int TILE = T * IPT;
-    uint32_t *s_keys = smem;
-    uint32_t *s_vals = smem + TILE;
-    uint32_t *s_cnt = smem + TILE * (PAIRS ? 2 : 1);   // [WARPS][256] counts, then next free slots
-    uint32_t *s_goff = s_cnt + WARPS * kRow;            // [256] global index - tile slot
-    uint32_t *s_misc = s_goff + 256;                    // [32]
+    uint32_t *s_cnt = tab;                      // [WARPS][256] counts, then next free slots
+    uint32_t *s_goff = s_cnt + WARPS * kRow;    // [256] global index - tile slot
+    uint32_t *s_misc = s_goff + 256;            // [32]
 
     const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t tile_base = tile * TILE;
@@ -262,7 +268,7 @@ __device__ __forceinline__ void pass_tile(const PassArgs &a, uint32_t *smem, uin
 #pragma unroll
     for (int k = 0; k < IPT; ++k) {
         const uint32_t i = item0 + k * 32;
-        key[k] = (FULL || i < tile_n) ? a.src_k[tile_base + i] : 0u;
+        key[k] = (FULL || i < tile_n) ? kin[i] : 0u;
         if (XIN) key[k] = float_key_in(key[k]);
     }
     uint32_t val[PAIRS ? IPT : 1];
@@ -270,7 +276,7 @@ __device__ __forceinline__ void pass_tile(const PassArgs &a, uint32_t *smem, uin
 #pragma unroll
         for (int k = 0; k < IPT; ++k) {
             const uint32_t i = item0 + k * 32;
-            val[k] = (FULL || i < tile_n) ? a.src_v[tile_base + i] : 0u;
+            val[k] = (FULL || i < tile_n) ? vin[i] : 0u;
         }
     }
 
@@ -359,7 +365,7 @@ __device__ __forceinline__ void pass_tile(const PassArgs &a, uint32_t *smem, uin
         }
     }
     __syncthreads();
-    if (s_misc[2] || tile == a.stall_tile) return;
+    if (s_misc[2] || tile == a.stall_tile) return false;
 
     // ---- contiguous runs per digit out to global memory
 #pragma unroll
@@ -374,6 +380,7 @@ __device__ __forceinline__ void pass_tile(const PassArgs &a, uint32_t *smem, uin
             }
         }
     }
+    return true;
 }
 
 template <int WARPS, int IPT, int MINB, int MATCH, bool BYTE, bool PAIRS, bool XIN, bool XOUT>
@@ -392,10 +399,107 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass(const PassArgs 
     __syncthreads();
     const uint32_t tile = s_misc[0];
     if (s_misc[1]) return;   // an earlier wait gave up; the result is void anyway
+    uint32_t *s_keys = smem, *s_vals = smem + TILE;
+    const uint32_t *kin = a.src_k + tile * TILE;
+    const uint32_t *vin = PAIRS ? a.src_v + tile * TILE : nullptr;
     if (a.n - tile * TILE >= static_cast<uint32_t>(TILE))
-        pass_tile<WARPS, IPT, MATCH, BYTE, PAIRS, XIN, XOUT, true>(a, smem, tile);
+        pass_tile<WARPS, IPT, MATCH, BYTE, PAIRS, XIN, XOUT, true>(a, s_cnt, tile, kin, vin, s_keys, s_vals);
     else
-        pass_tile<WARPS, IPT, MATCH, BYTE, PAIRS, XIN, XOUT, false>(a, smem, tile);
+        pass_tile<WARPS, IPT, MATCH, BYTE, PAIRS, XIN, XOUT, false>(a, s_cnt, tile, kin, vin, s_keys, s_vals);
+}
+
+// ------------------------------------------------- persistent digit pass
+// A grid of (resident) CTAs loops over tiles.  While it processes tile k from
+// one shared buffer, the next tile it claimed is already on its way into the
+// other buffer through a TMA bulk copy, so neither the tile-id claim nor the
+// key loads wait on memory.  Tiles are still claimed in increasing order, and
+// each CTA processes its tiles in that order, so the smallest unfinished tile
+// can always complete: the look-back keeps making progress.
+constexpr uint32_t kBulkWaitLimit = 1u << 20;   // polls of a load barrier before giving up
+
+template <int WARPS, int IPT, bool PAIRS>
+constexpr size_t persist_smem_words() {
+    // 2 barriers (padded to 32 words), 2 key buffers [, 2 value buffers], tables
+    return 32 + static_cast<size_t>(WARPS * 32 * IPT) * (PAIRS ? 4 : 2) + WARPS * kRow + 256 + 32;
+}
+
+template <int WARPS, int IPT, int MATCH, bool BYTE, bool PAIRS, bool XIN, bool XOUT>
+__global__ void __launch_bounds__(WARPS * 32, 2) k_digit_pass_persistent(const PassArgs a,
+                                                                        uint32_t tiles) {
+    constexpr int T = WARPS * 32;
+    constexpr int TILE = T * IPT;
+    extern __shared__ __align__(128) uint32_t smem[];
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem);          // [2]
+    uint32_t *kbuf = smem + 32;                                   // [2][TILE]
+    uint32_t *vbuf = kbuf + 2 * TILE;                             // [2][TILE] (pairs)
+    uint32_t *tab = smem + 32 + static_cast<size_t>(TILE) * (PAIRS ? 4 : 2);
+    uint32_t *s_misc = tab + WARPS * kRow + 256;
+    const uint32_t tid = threadIdx.x;
+
+    // Issues the bulk copy of tile t into buffer b (thread 0 only).
+    auto prefetch = [&](uint32_t t, uint32_t b) {
+        const uint32_t n_t = min(static_cast<uint32_t>(TILE), a.n - t * TILE);
+        const uint32_t bytes = (n_t & ~3u) * 4u;
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&bar[b], bytes * (PAIRS ? 2u : 1u));
+        if (bytes > 0) {
+            bulk_load(kbuf + b * TILE, a.src_k + t * TILE, bytes, &bar[b]);
+            if (PAIRS) bulk_load(vbuf + b * TILE, a.src_v + t * TILE, bytes, &bar[b]);
+        }
+    };
+
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        const uint32_t t0 = atomicAdd(a.tile_counter, 1u);
+        s_misc[24] = t0;
+        if (t0 < tiles) prefetch(t0, 0);
+    }
+    __syncthreads();
+    uint32_t tile = s_misc[24];   // its copy into buffer b is in flight if tile < tiles
+    uint32_t b = 0;
+    uint32_t phase[2] = {0u, 0u};
+    while (tile < tiles) {
+        // claim the next tile and start its copy into the other buffer
+        if (tid == 0) {
+            const uint32_t next = atomicAdd(a.tile_counter, 1u);
+            s_misc[24] = next;
+            if (next < tiles) prefetch(next, b ^ 1u);
+            s_misc[2] = 0;
+        }
+        for (uint32_t i = tid; i < WARPS * kRow; i += T) tab[i] = 0;
+        const bool arrived = mbar_wait_bounded(&bar[b], phase[b], kBulkWaitLimit);
+        const uint32_t tile_n = min(static_cast<uint32_t>(TILE), a.n - tile * TILE);
+        uint32_t *kb = kbuf + b * TILE;
+        uint32_t *vb = vbuf + b * TILE;
+        const uint32_t rest = tile_n & 3u;   // the last keys of a ragged tile come by plain loads
+        if (arrived && tid < rest) {
+            kb[tile_n - rest + tid] = a.src_k[tile * TILE + tile_n - rest + tid];
+            if (PAIRS) vb[tile_n - rest + tid] = a.src_v[tile * TILE + tile_n - rest + tid];
+        }
+        const bool quit = __syncthreads_or(!arrived || (tid == 0 && ld_relaxed(a.abort_flag) != 0));
+        const uint32_t next = s_misc[24];
+        if (quit) {
+            // the result is void; leave only once no copy into this block is in flight
+            if (tid == 0 && !arrived) record_error(a.status, a.abort_flag, GSORT_ETIMEOUT);
+            if (!arrived) mbar_wait_bounded(&bar[b], phase[b], kBulkWaitLimit);
+            if (next < tiles) mbar_wait_bounded(&bar[b ^ 1u], phase[b ^ 1u], kBulkWaitLimit);
+            return;
+        }
+        phase[b] ^= 1u;
+        bool ok;
+        if (tile_n == static_cast<uint32_t>(TILE))
+            ok = pass_tile<WARPS, IPT, MATCH, BYTE, PAIRS, XIN, XOUT, true>(a, tab, tile, kb, vb, kb, vb);
+        else
+            ok = pass_tile<WARPS, IPT, MATCH, BYTE, PAIRS, XIN, XOUT, false>(a, tab, tile, kb, vb, kb, vb);
+        __syncthreads();   // buffer b is read out before the next copy into it
+        if (!ok && tile != a.stall_tile) {   // a look-back gave up
+            if (next < tiles) mbar_wait_bounded(&bar[b ^ 1u], phase[b ^ 1u], kBulkWaitLimit);
+            return;
+        }
+        tile = next;
+        b ^= 1u;
+    }
 }
 
 // ------------------------------------------------------------ variants
@@ -438,6 +542,60 @@ struct PassConfig {
     }
 };
 
+// Persistent configuration: grid = 2 CTAs per SM (at most one per tile).
+// Sources that are not 16-byte aligned take the one-tile-per-CTA kernel with
+// the same tile shape.
+template <int WARPS, int IPT, int MATCH>
+struct PersistentConfig {
+    static constexpr uint32_t kTile = WARPS * 32 * IPT;
+
+    template <bool B, bool P, bool XI, bool XO>
+    static cudaError_t launch_one(const PassArgs &a, uint32_t tiles, cudaStream_t s) {
+        auto k = k_digit_pass_persistent<WARPS, IPT, MATCH, B, P, XI, XO>;
+        const size_t smem = persist_smem_words<WARPS, IPT, P>() * sizeof(uint32_t);
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, WARPS * 32, smem);
+        if (e != cudaSuccess) return e;
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return cudaErrorUnknown;
+        const uint32_t grid = std::max(1u, std::min(tiles, static_cast<uint32_t>(std::max(per_sm, 1) * sms)));
+        k<<<grid, WARPS * 32, smem, s>>>(a, tiles);
+        return cudaGetLastError();
+    }
+
+    template <bool B>
+    static cudaError_t launch_b(const PassArgs &a, bool pairs, bool xin, bool xout, uint32_t tiles,
+                                cudaStream_t s) {
+        const int sel = (pairs ? 4 : 0) | (xin ? 2 : 0) | (xout ? 1 : 0);
+        switch (sel) {
+            case 0: return launch_one<B, false, false, false>(a, tiles, s);
+            case 1: return launch_one<B, false, false, true>(a, tiles, s);
+            case 2: return launch_one<B, false, true, false>(a, tiles, s);
+            case 3: return launch_one<B, false, true, true>(a, tiles, s);
+            case 4: return launch_one<B, true, false, false>(a, tiles, s);
+            case 5: return launch_one<B, true, false, true>(a, tiles, s);
+            case 6: return launch_one<B, true, true, false>(a, tiles, s);
+            default: return launch_one<B, true, true, true>(a, tiles, s);
+        }
+    }
+
+    static cudaError_t launch(const PassArgs &a, bool pairs, bool xin, bool xout, uint32_t tiles,
+                              cudaStream_t s) {
+        const bool aligned16 = (reinterpret_cast<uintptr_t>(a.src_k) & 15) == 0 &&
+                               (!pairs || (reinterpret_cast<uintptr_t>(a.src_v) & 15) == 0);
+        if (!aligned16)
+            return PassConfig<WARPS, IPT, 2, MATCH>::launch(a, pairs, xin, xout, tiles, s);
+        const bool byte = (a.shift % 8) == 0 && a.mask == 0xFFu;
+        return byte ? launch_b<true>(a, pairs, xin, xout, tiles, s)
+                    : launch_b<false>(a, pairs, xin, xout, tiles, s);
+    }
+};
+
 struct Variant {
     const char *name;
     uint32_t tile;
@@ -445,13 +603,11 @@ struct Variant {
 };
 
 const Variant kVariants[] = {
-    {"16 warps x 16 items, ballot tables", PassConfig<16, 16, 2, kMatchTable>::kTile,
+    {"one tile per CTA, 16 warps x 16 items", PassConfig<16, 16, 2, kMatchTable>::kTile,
      &PassConfig<16, 16, 2, kMatchTable>::launch},
-    {"16 warps x 16 items, ballot select", PassConfig<16, 16, 2, kMatchSelect>::kTile,
-     &PassConfig<16, 16, 2, kMatchSelect>::launch},
-    {"16 warps x 16 items, match.any", PassConfig<16, 16, 2, kMatchAny>::kTile,
-     &PassConfig<16, 16, 2, kMatchAny>::launch},
-    {"8 warps x 16 items, ballot tables", PassConfig<8, 16, 3, kMatchTable>::kTile,
+    {"persistent, 16 warps x 16 items, TMA prefetch", PersistentConfig<16, 16, kMatchTable>::kTile,
+     &PersistentConfig<16, 16, kMatchTable>::launch},
+    {"one tile per CTA, 8 warps x 16 items", PassConfig<8, 16, 3, kMatchTable>::kTile,
      &PassConfig<8, 16, 3, kMatchTable>::launch},
 };
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
