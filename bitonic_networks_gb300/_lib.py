@@ -58,6 +58,9 @@ SIGNATURES = {
                                                  ctypes.c_int64, ctypes.c_void_p,
                                                  ctypes.c_void_p, ctypes.c_size_t,
                                                  ctypes.c_void_p, ctypes.POINTER(Options)]),
+    "gsort_compact_positive_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p,
+                                                      ctypes.c_int64, ctypes.c_void_p,
+                                                      ctypes.c_void_p]),
     "gsort_segmented_bitonic": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
                                                ctypes.c_void_p]),
     "gsort_check": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),

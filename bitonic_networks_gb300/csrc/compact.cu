@@ -10,6 +10,7 @@
 // kernel writes +0.0 to out[m..n) (the pages' worked example shows a zero
 // tail; their kernels leave it unwritten).  Traffic: read 4n, write 4n.
 #include <algorithm>
+#include <mutex>
 
 #include "gsort_internal.cuh"
 
@@ -209,3 +210,88 @@ int launch_compact(const CompactLaunch &L) {
 }
 
 }  // namespace gsort
+
+// ------------------------------------------------ allocation-free variant
+// Some callers cannot hand this library a workspace: code that runs where
+// device allocation is forbidden or too costly, such as the execute step of a
+// plugin whose host framework owns all device memory, a real-time loop that
+// cannot afford cudaMalloc's device-wide synchronisation and unbounded
+// latency, or a handler that runs while the caller's own allocator is busy.
+// For them, gsort_compact_positive_noalloc keeps its scratch (status words,
+// tile counter, kept count and one look-back word per tile) in the static
+// device array below, sized for GSORT_COMPACT_NOALLOC_MAX_N elements.  Every
+// GPU that loads the library holds this array until the process exits.
+namespace {
+
+constexpr uint32_t kNoAllocMaxN = GSORT_COMPACT_NOALLOC_MAX_N;
+// the compaction workspace for kNoAllocMaxN elements: header + one word per tile
+constexpr size_t kNoAllocScratchBytes =
+    gsort::kHdrBytes +
+    ((kNoAllocMaxN + gsort::kCompactTile - 1) / gsort::kCompactTile * 4u + 255u) / 256u * 256u;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 256;
+std::mutex g_noalloc_mutex;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the static scratch on device `dev` (the current device).
+// The first call on a device asks the runtime for it; later calls reuse it.
+int noalloc_scratch(int dev, void **out) {
+    if (dev < 0 || dev >= kMaxDevices) return GSORT_EINVAL;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+            return GSORT_ECUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return GSORT_OK;
+}
+
+}  // namespace
+
+extern "C" int gsort_compact_positive_noalloc(const float *d_in, float *d_out, int64_t n,
+                                              int64_t *d_num_kept, cudaStream_t stream) {
+    using namespace gsort;
+    if (n < 0) return GSORT_EINVAL;
+    if (n > static_cast<int64_t>(kNoAllocMaxN)) return GSORT_ETOOBIG;
+    if (d_num_kept != nullptr && (reinterpret_cast<uintptr_t>(d_num_kept) & 7) != 0)
+        return GSORT_EALIGN;
+    if (n > 0) {
+        if (d_in == nullptr || d_out == nullptr) return GSORT_EINVAL;
+        if ((reinterpret_cast<uintptr_t>(d_in) & 3) != 0 || (reinterpret_cast<uintptr_t>(d_out) & 3) != 0)
+            return GSORT_EALIGN;
+        const uintptr_t a = reinterpret_cast<uintptr_t>(d_in), b = reinterpret_cast<uintptr_t>(d_out);
+        const uintptr_t bytes = static_cast<uintptr_t>(n) * 4;
+        if (a < b + bytes && b < a + bytes) return GSORT_EINVAL;
+    }
+    DeviceInfo dev;
+    if (device_info(&dev) != GSORT_OK) return GSORT_ECUDA;
+    if (compact_layout(static_cast<uint32_t>(n)).total > kNoAllocScratchBytes) return GSORT_ETOOBIG;
+    void *scratch = nullptr;
+    const int rc = noalloc_scratch(dev.device, &scratch);
+    if (rc != GSORT_OK) return rc;
+    if (n == 0) {
+        if (d_num_kept != nullptr &&
+            cudaMemsetAsync(d_num_kept, 0, sizeof(int64_t), stream) != cudaSuccess)
+            return GSORT_ECUDA;
+        return GSORT_OK;
+    }
+    // the compaction's own init kernel clears the header and the look-back
+    // words at the start of the call, so the array's old contents do not matter
+    CompactLaunch L;
+    L.in = reinterpret_cast<const uint32_t *>(d_in);
+    L.out = reinterpret_cast<uint32_t *>(d_out);
+    L.n = static_cast<uint32_t>(n);
+    L.num_kept = d_num_kept;
+    L.ws = static_cast<unsigned char *>(scratch);
+    L.spin_limit = kDefaultSpinLimit;
+    L.stall_tile = kNoStall;
+    L.events = nullptr;
+    L.num_events = 0;
+    L.stream = stream;
+    L.sm_count = dev.sm_count;
+    return launch_compact(L);
+}

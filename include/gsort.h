@@ -135,6 +135,31 @@ int gsort_compact_positive(const float *d_in, float *d_out, int64_t n,
                            cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Allocation-free compaction.  The reference pages have no counterpart: this
+ * call exists for callers that cannot provide a workspace, because they run
+ * where device allocation is forbidden or too costly (the execute step of a
+ * plugin whose host framework owns all device memory, a real-time loop that
+ * cannot afford cudaMalloc's device-wide synchronisation and latency, a
+ * handler that runs while the caller's allocator is busy).
+ *
+ * Same result as gsort_compact_positive, for 0 <= n <=
+ * GSORT_COMPACT_NOALLOC_MAX_N (larger: GSORT_ETOOBIG).  The caller still
+ * passes the input, the output and the optional kept count.  The scratch is
+ * one static device array inside the library (about 136 KiB), which every GPU
+ * that loads the library keeps until the process exits; this call allocates
+ * nothing.  The first call on a device looks up that array's device address
+ * (make that first call before any stream capture); later calls reuse it.
+ * All calls share the array: calls whose work overlaps on the GPU (for
+ * example on two streams at once) race and corrupt each other's results, so
+ * serialise them.  A device-side look-back timeout, which does not occur in
+ * normal operation, leaves the output undefined and is not reported here.
+ * ---------------------------------------------------------------------- */
+#define GSORT_COMPACT_NOALLOC_MAX_N ((int64_t)1 << 28)
+
+int gsort_compact_positive_noalloc(const float *d_in, float *d_out, int64_t n,
+                                   int64_t *d_num_kept, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Segmented bitonic sort  ([GPUSORT] sort of <=1024 elements in one block;
  * [PMPP10] 10.2)
  *
