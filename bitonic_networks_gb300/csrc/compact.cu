@@ -5,8 +5,8 @@
 //
 // One kernel reads every tile once: predicate, block scan of the per-thread
 // counts, publish the tile count, look back (warp 0 inspects 32 earlier tiles
-// per step), stage the kept values of the tile contiguously in shared memory
-// and copy them out as one run.  The last tile records the total m; a second
+// per step, while the other warps stage the tile's kept values contiguously in
+// shared memory) and copy the kept values out as one run.  The last tile records the total m; a second
 // kernel writes +0.0 to out[m..n) (the pages' worked example shows a zero
 // tail; their kernels leave it unwritten).  Traffic: read 4n, write 4n.
 #include <algorithm>
@@ -20,6 +20,11 @@ namespace {
 constexpr int kCompactThreads = 512;
 constexpr int kCompactItems = 16;          // per thread, a multiple of 4
 constexpr uint32_t kCompactTile = kCompactThreads * kCompactItems;
+constexpr int kCompactLookChunks = 1;      // look-back window: 32 predecessor tiles per round
+// One look-back word per 128-byte line: hundreds of waiting tiles poll their
+// predecessors' words at once, and packing the words densely puts all of that
+// polling on a few L2 lines.  Spread out, the polls of one window hit 32 lines.
+constexpr uint32_t kStateStride = 32;      // words
 
 __global__ void k_zero_words(uint32_t *p, uint32_t nwords) {
     for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < nwords;
@@ -78,50 +83,68 @@ k_compact(const uint32_t *__restrict__ in, uint32_t *__restrict__ out, uint32_t 
     for (int j = 0; j < IPT; ++j) flags |= is_positive(x[j]) << j;
     const uint32_t cnt = __popc(flags);
 
-    // block exclusive scan of the per-thread counts
+    // block exclusive scan of the per-thread counts: warp scans, then every
+    // thread adds up the totals of the warps before its own (one barrier)
     const uint32_t incl = warp_inclusive_scan(cnt, lane);
     if (lane == 31) s_warp[warp] = incl;
     __syncthreads();
-    if (warp == 0) {
-        const uint32_t w = lane < WARPS ? s_warp[lane] : 0u;
-        const uint32_t wi = warp_inclusive_scan(w, lane);
-        if (lane < WARPS) s_warp[lane] = wi - w;
-        if (lane == WARPS - 1) s_misc[2] = wi;   // tile total
+    uint32_t warp_excl = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) {
+        const uint32_t c = s_warp[w];
+        warp_excl += (static_cast<uint32_t>(w) < warp) ? c : 0u;
+        total += c;
     }
-    __syncthreads();
-    const uint32_t total = s_misc[2];
-    uint32_t pos = s_warp[warp] + incl - cnt;
+    uint32_t pos = warp_excl + incl - cnt;
 
-    // decoupled look-back by warp 0: lane l inspects tile (t - 1 - l)
     if (warp == 0) {
+        // publish the tile count at once, then look back: lane l inspects tile (t - 1 - l)
         uint32_t prefix = 0;
         bool ok = true;
         if (lane == 0 && tile != stall_tile)
-            st_relaxed(states + tile, (tile == 0 ? kFlagPrefix : kFlagAgg) | total);
+            st_relaxed(states + tile * kStateStride, (tile == 0 ? kFlagPrefix : kFlagAgg) | total);
         if (tile > 0 && tile != stall_tile) {
+            // a round reads 4 x 32 predecessors: lane l of chunk q inspects tile t - 32q - l
             int32_t t = static_cast<int32_t>(tile) - 1 - static_cast<int32_t>(lane);
             uint32_t polls = 0, ns = 32;
             while (true) {
-                // before tile 0 sits an empty prefix
-                const uint32_t s = (t >= 0) ? ld_relaxed(states + t) : kFlagPrefix;
-                const uint32_t flag = s & ~kValueMask;
-                const uint32_t pmask = __ballot_sync(kFullMask, flag == kFlagPrefix);
-                const uint32_t zmask = __ballot_sync(kFullMask, flag == 0);
-                // lanes up to and including the nearest published prefix matter
-                const uint32_t need = pmask ? (((pmask & (0u - pmask)) << 1) - 1u) : kFullMask;
-                if (zmask & need) {
+                uint32_t s[kCompactLookChunks];
+#pragma unroll
+                for (int q = 0; q < kCompactLookChunks; ++q) {
+                    const int32_t tq = t - 32 * q;
+                    s[q] = (tq >= 0) ? ld_relaxed(states + tq * kStateStride) : kFlagPrefix;   // empty prefix before tile 0
+                }
+                bool pending = false, found = false;
+                uint32_t sum = 0;
+#pragma unroll
+                for (int q = 0; q < kCompactLookChunks; ++q) {
+                    if (!found && !pending) {
+                        const uint32_t flag = s[q] & ~kValueMask;
+                        const uint32_t pmask = __ballot_sync(kFullMask, flag == kFlagPrefix);
+                        const uint32_t zmask = __ballot_sync(kFullMask, flag == 0);
+                        // lanes up to and including the nearest published prefix matter
+                        const uint32_t need = pmask ? (((pmask & (0u - pmask)) << 1) - 1u) : kFullMask;
+                        if (zmask & need) {
+                            pending = true;
+                        } else {
+                            sum += __reduce_add_sync(kFullMask, ((need >> lane) & 1u) ? (s[q] & kValueMask) : 0u);
+                            found = pmask != 0;
+                        }
+                    }
+                }
+                if (pending) {
                     ++polls;
                     const bool give_up = __any_sync(kFullMask, polls >= spin_limit ||
                                                                    ld_relaxed(abort_flag) != 0);
                     if (give_up) { ok = false; break; }
                     backoff(ns);
-                    continue;
+                    continue;   // re-read the whole window
                 }
-                prefix += __reduce_add_sync(kFullMask, ((need >> lane) & 1u) ? (s & kValueMask) : 0u);
-                if (pmask) break;
-                t -= 32;
+                prefix += sum;
+                if (found) break;
+                t -= 32 * kCompactLookChunks;
             }
-            if (ok && lane == 0) st_relaxed(states + tile, kFlagPrefix | (prefix + total));
+            if (ok && lane == 0) st_relaxed(states + tile * kStateStride, kFlagPrefix | (prefix + total));
         }
         if (lane == 0) {
             s_misc[1] = ok ? 0u : 1u;
@@ -129,15 +152,16 @@ k_compact(const uint32_t *__restrict__ in, uint32_t *__restrict__ out, uint32_t 
             if (!ok) record_error(status, abort_flag, GSORT_ETIMEOUT);
         }
     }
-    __syncthreads();
-    if (s_misc[1] || tile == stall_tile) return;
-    const uint32_t prefix = s_misc[3];
 
-    // stage the kept values contiguously, then copy them out as one run
+    // stage the kept values contiguously (overlaps warp 0's look-back)
 #pragma unroll
     for (int j = 0; j < IPT; ++j)
         if ((flags >> j) & 1u) s_buf[pos++] = x[j];
     __syncthreads();
+    if (s_misc[1] || tile == stall_tile) return;
+    const uint32_t prefix = s_misc[3];
+
+    // copy them out as one run
     for (uint32_t i = tid; i < total; i += T) {
         const uint32_t g = prefix + i;
         if (g < n) out[g] = s_buf[i];
@@ -148,7 +172,10 @@ k_compact(const uint32_t *__restrict__ in, uint32_t *__restrict__ out, uint32_t 
 // +0.0 into out[m..n), m read from the workspace; also reports m.
 __global__ void k_zero_tail(uint32_t *out, uint32_t n, const unsigned long long *kept,
                             int64_t *num_kept) {
-    const uint32_t m = static_cast<uint32_t>(min(*kept, static_cast<unsigned long long>(n)));
+    __shared__ uint32_t s_m;
+    if (threadIdx.x == 0) s_m = static_cast<uint32_t>(min(*kept, static_cast<unsigned long long>(n)));
+    __syncthreads();
+    const uint32_t m = s_m;
     if (blockIdx.x == 0 && threadIdx.x == 0 && num_kept != nullptr)
         *num_kept = static_cast<int64_t>(m);
     const uint32_t gtid = blockIdx.x * blockDim.x + threadIdx.x;
@@ -174,7 +201,7 @@ CompactLayout compact_layout(uint32_t n) {
     CompactLayout L{};
     L.tiles = (n + kCompactTile - 1) / kCompactTile;
     L.states = kHdrBytes;
-    L.total = kHdrBytes + align_up(static_cast<size_t>(L.tiles) * sizeof(uint32_t), kWsAlign);
+    L.total = kHdrBytes + align_up(static_cast<size_t>(L.tiles) * kStateStride * sizeof(uint32_t), kWsAlign);
     return L;
 }
 
@@ -189,7 +216,7 @@ int launch_compact(const CompactLaunch &L) {
     uint32_t *states = reinterpret_cast<uint32_t *>(L.ws + lay.states);
 
     record(L.events, L.num_events, 0, s);
-    const uint32_t init_words = static_cast<uint32_t>(kHdrBytes / 4) + lay.tiles;
+    const uint32_t init_words = static_cast<uint32_t>(kHdrBytes / 4) + lay.tiles * kStateStride;
     const uint32_t init_grid = std::min<uint32_t>((init_words + 1023) / 1024, 4u * L.sm_count);
     k_zero_words<<<init_grid, 256, 0, s>>>(words, init_words);
     if (cudaGetLastError() != cudaSuccess) return GSORT_ECUDA;
@@ -218,16 +245,18 @@ int launch_compact(const CompactLaunch &L) {
 // cannot afford cudaMalloc's device-wide synchronisation and unbounded
 // latency, or a handler that runs while the caller's own allocator is busy.
 // For them, gsort_compact_positive_noalloc keeps its scratch (status words,
-// tile counter, kept count and one look-back word per tile) in the static
-// device array below, sized for GSORT_COMPACT_NOALLOC_MAX_N elements.  Every
+// tile counter, kept count and one look-back line per tile) in the static
+// device array below (about 4 MiB), sized for GSORT_COMPACT_NOALLOC_MAX_N elements.  Every
 // GPU that loads the library holds this array until the process exits.
 namespace {
 
 constexpr uint32_t kNoAllocMaxN = GSORT_COMPACT_NOALLOC_MAX_N;
-// the compaction workspace for kNoAllocMaxN elements: header + one word per tile
+// the compaction workspace for kNoAllocMaxN elements: header + one 128-byte
+// look-back line per tile
 constexpr size_t kNoAllocScratchBytes =
     gsort::kHdrBytes +
-    ((kNoAllocMaxN + gsort::kCompactTile - 1) / gsort::kCompactTile * 4u + 255u) / 256u * 256u;
+    ((kNoAllocMaxN + gsort::kCompactTile - 1) / gsort::kCompactTile * gsort::kStateStride * 4u + 255u) /
+        256u * 256u;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 

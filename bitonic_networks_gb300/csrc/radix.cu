@@ -199,22 +199,22 @@ constexpr size_t pass_smem_words() {
     return static_cast<size_t>(WARPS * 32 * IPT) * (PAIRS ? 2 : 1) + WARPS * kRow + 256 + 32;
 }
 
-constexpr int kLookWindow = 8;   // predecessor tiles read per look-back round
 
 // Exclusive prefix of digit d over all tiles before `tile`.  Each word holds a
 // flag (AGG: the tile's count; PREFIX: the count over tiles 0..t) and a
-// 30-bit count, so one round trip reads kLookWindow predecessors at once; the
+// 30-bit count, so one round trip reads W predecessors at once; the
 // nearest PREFIX word ends the walk and the AGG words before it are summed.
 // Returns false if a wait gave up.
+template <int W>
 __device__ __forceinline__ bool look_back(const PassArgs &a, uint32_t tile, uint32_t d,
                                           uint32_t &excl) {
     excl = 0;
     int32_t t = static_cast<int32_t>(tile) - 1;
     uint32_t polls = 0, ns = 32;
     while (true) {
-        uint32_t w[kLookWindow];
+        uint32_t w[W];
 #pragma unroll
-        for (int i = 0; i < kLookWindow; ++i)
+        for (int i = 0; i < W; ++i)
             w[i] = (t - i >= 0) ? ld_relaxed(a.look + static_cast<uint32_t>(t - i) * 256 + d)
                                 : kFlagPrefix;   // before tile 0: an empty prefix
         // sum words up to and including the nearest PREFIX; any empty word
@@ -222,7 +222,7 @@ __device__ __forceinline__ bool look_back(const PassArgs &a, uint32_t tile, uint
         uint32_t sum = 0;
         bool done = false, pending = false;
 #pragma unroll
-        for (int i = 0; i < kLookWindow; ++i) {
+        for (int i = 0; i < W; ++i) {
             if (!done) {
                 pending |= (w[i] & ~kValueMask) == 0;
                 sum += w[i] & kValueMask;
@@ -236,7 +236,7 @@ __device__ __forceinline__ bool look_back(const PassArgs &a, uint32_t tile, uint
         }
         excl += sum;
         if (done) return true;
-        t -= kLookWindow;
+        t -= W;
     }
 }
 
@@ -246,7 +246,7 @@ __device__ __forceinline__ bool look_back(const PassArgs &a, uint32_t tile, uint
 // registers before the first write).  tab = the shared tables: per-warp digit
 // counters, digit offsets, misc words.  Returns false when the tile stops
 // (device error or the test stall), after a block barrier.
-template <int WARPS, int IPT, int MATCH, bool BYTE, bool PAIRS, bool XIN, bool XOUT, bool FULL>
+template <int WARPS, int IPT, int MATCH, int LW, bool BYTE, bool PAIRS, bool XIN, bool XOUT, bool FULL>
 __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, uint32_t tile,
                                           const uint32_t *kin, const uint32_t *vin,
                                           uint32_t *s_keys, uint32_t *s_vals) {
@@ -330,7 +330,7 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, uint
         uint32_t excl = 0;
         bool ok = true;
         if (tile > 0 && tile != a.stall_tile) {
-            ok = look_back(a, tile, tid, excl);
+            ok = look_back<LW>(a, tile, tid, excl);
             if (ok) st_relaxed(a.look + tile * 256 + tid, kFlagPrefix | (excl + cnt));
         }
         if (!ok) {
@@ -383,7 +383,7 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, uint
     return true;
 }
 
-template <int WARPS, int IPT, int MINB, int MATCH, bool BYTE, bool PAIRS, bool XIN, bool XOUT>
+template <int WARPS, int IPT, int MINB, int MATCH, int LW, bool BYTE, bool PAIRS, bool XIN, bool XOUT>
 __global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass(const PassArgs a) {
     constexpr int TILE = WARPS * 32 * IPT;
     extern __shared__ uint32_t smem[];
@@ -403,9 +403,9 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass(const PassArgs 
     const uint32_t *kin = a.src_k + tile * TILE;
     const uint32_t *vin = PAIRS ? a.src_v + tile * TILE : nullptr;
     if (a.n - tile * TILE >= static_cast<uint32_t>(TILE))
-        pass_tile<WARPS, IPT, MATCH, BYTE, PAIRS, XIN, XOUT, true>(a, s_cnt, tile, kin, vin, s_keys, s_vals);
+        pass_tile<WARPS, IPT, MATCH, LW, BYTE, PAIRS, XIN, XOUT, true>(a, s_cnt, tile, kin, vin, s_keys, s_vals);
     else
-        pass_tile<WARPS, IPT, MATCH, BYTE, PAIRS, XIN, XOUT, false>(a, s_cnt, tile, kin, vin, s_keys, s_vals);
+        pass_tile<WARPS, IPT, MATCH, LW, BYTE, PAIRS, XIN, XOUT, false>(a, s_cnt, tile, kin, vin, s_keys, s_vals);
 }
 
 // ------------------------------------------------- persistent digit pass
@@ -423,7 +423,7 @@ constexpr size_t persist_smem_words() {
     return 32 + static_cast<size_t>(WARPS * 32 * IPT) * (PAIRS ? 4 : 2) + WARPS * kRow + 256 + 32;
 }
 
-template <int WARPS, int IPT, int MATCH, bool BYTE, bool PAIRS, bool XIN, bool XOUT>
+template <int WARPS, int IPT, int MATCH, int LW, bool BYTE, bool PAIRS, bool XIN, bool XOUT>
 __global__ void __launch_bounds__(WARPS * 32, 2) k_digit_pass_persistent(const PassArgs a,
                                                                         uint32_t tiles) {
     constexpr int T = WARPS * 32;
@@ -489,9 +489,9 @@ __global__ void __launch_bounds__(WARPS * 32, 2) k_digit_pass_persistent(const P
         phase[b] ^= 1u;
         bool ok;
         if (tile_n == static_cast<uint32_t>(TILE))
-            ok = pass_tile<WARPS, IPT, MATCH, BYTE, PAIRS, XIN, XOUT, true>(a, tab, tile, kb, vb, kb, vb);
+            ok = pass_tile<WARPS, IPT, MATCH, LW, BYTE, PAIRS, XIN, XOUT, true>(a, tab, tile, kb, vb, kb, vb);
         else
-            ok = pass_tile<WARPS, IPT, MATCH, BYTE, PAIRS, XIN, XOUT, false>(a, tab, tile, kb, vb, kb, vb);
+            ok = pass_tile<WARPS, IPT, MATCH, LW, BYTE, PAIRS, XIN, XOUT, false>(a, tab, tile, kb, vb, kb, vb);
         __syncthreads();   // buffer b is read out before the next copy into it
         if (!ok && tile != a.stall_tile) {   // a look-back gave up
             if (next < tiles) mbar_wait_bounded(&bar[b ^ 1u], phase[b ^ 1u], kBulkWaitLimit);
@@ -503,13 +503,13 @@ __global__ void __launch_bounds__(WARPS * 32, 2) k_digit_pass_persistent(const P
 }
 
 // ------------------------------------------------------------ variants
-template <int WARPS, int IPT, int MINB, int MATCH>
+template <int WARPS, int IPT, int MINB, int MATCH, int LW = 8>
 struct PassConfig {
     static constexpr uint32_t kTile = WARPS * 32 * IPT;
 
     template <bool B, bool P, bool XI, bool XO>
     static cudaError_t launch_one(const PassArgs &a, uint32_t tiles, cudaStream_t s) {
-        auto k = k_digit_pass<WARPS, IPT, MINB, MATCH, B, P, XI, XO>;
+        auto k = k_digit_pass<WARPS, IPT, MINB, MATCH, LW, B, P, XI, XO>;
         const size_t smem = pass_smem_words<WARPS, IPT, P>() * sizeof(uint32_t);
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
@@ -545,13 +545,13 @@ struct PassConfig {
 // Persistent configuration: grid = 2 CTAs per SM (at most one per tile).
 // Sources that are not 16-byte aligned take the one-tile-per-CTA kernel with
 // the same tile shape.
-template <int WARPS, int IPT, int MATCH>
+template <int WARPS, int IPT, int MATCH, int LW = 8>
 struct PersistentConfig {
     static constexpr uint32_t kTile = WARPS * 32 * IPT;
 
     template <bool B, bool P, bool XI, bool XO>
     static cudaError_t launch_one(const PassArgs &a, uint32_t tiles, cudaStream_t s) {
-        auto k = k_digit_pass_persistent<WARPS, IPT, MATCH, B, P, XI, XO>;
+        auto k = k_digit_pass_persistent<WARPS, IPT, MATCH, LW, B, P, XI, XO>;
         const size_t smem = persist_smem_words<WARPS, IPT, P>() * sizeof(uint32_t);
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
@@ -589,7 +589,7 @@ struct PersistentConfig {
         const bool aligned16 = (reinterpret_cast<uintptr_t>(a.src_k) & 15) == 0 &&
                                (!pairs || (reinterpret_cast<uintptr_t>(a.src_v) & 15) == 0);
         if (!aligned16)
-            return PassConfig<WARPS, IPT, 2, MATCH>::launch(a, pairs, xin, xout, tiles, s);
+            return PassConfig<WARPS, IPT, 2, MATCH, LW>::launch(a, pairs, xin, xout, tiles, s);
         const bool byte = (a.shift % 8) == 0 && a.mask == 0xFFu;
         return byte ? launch_b<true>(a, pairs, xin, xout, tiles, s)
                     : launch_b<false>(a, pairs, xin, xout, tiles, s);
@@ -603,12 +603,16 @@ struct Variant {
 };
 
 const Variant kVariants[] = {
-    {"one tile per CTA, 16 warps x 16 items", PassConfig<16, 16, 2, kMatchTable>::kTile,
-     &PassConfig<16, 16, 2, kMatchTable>::launch},
+    {"one tile per CTA, 16 warps x 16 items, look-back window 8", PassConfig<16, 16, 2, kMatchTable, 8>::kTile,
+     &PassConfig<16, 16, 2, kMatchTable, 8>::launch},
     {"persistent, 16 warps x 16 items, TMA prefetch", PersistentConfig<16, 16, kMatchTable>::kTile,
      &PersistentConfig<16, 16, kMatchTable>::launch},
     {"one tile per CTA, 8 warps x 16 items", PassConfig<8, 16, 3, kMatchTable>::kTile,
      &PassConfig<8, 16, 3, kMatchTable>::launch},
+    {"one tile per CTA, 16 warps x 16 items, look-back window 16", PassConfig<16, 16, 2, kMatchTable, 16>::kTile,
+     &PassConfig<16, 16, 2, kMatchTable, 16>::launch},
+    {"one tile per CTA, 16 warps x 16 items, look-back window 4", PassConfig<16, 16, 2, kMatchTable, 4>::kTile,
+     &PassConfig<16, 16, 2, kMatchTable, 4>::launch},
 };
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 

@@ -145,7 +145,7 @@ int gsort_compact_positive(const float *d_in, float *d_out, int64_t n,
  * Same result as gsort_compact_positive, for 0 <= n <=
  * GSORT_COMPACT_NOALLOC_MAX_N (larger: GSORT_ETOOBIG).  The caller still
  * passes the input, the output and the optional kept count.  The scratch is
- * one static device array inside the library (about 136 KiB), which every GPU
+ * one static device array inside the library (about 4 MiB), which every GPU
  * that loads the library keeps until the process exits; this call allocates
  * nothing.  The first call on a device looks up that array's device address
  * (make that first call before any stream capture); later calls reuse it.

@@ -64,7 +64,7 @@ def test_workspace_sizes(lib):
         assert lib.gsort_radix_workspace_bytes(n, 0) == HDR + state + keys
         assert lib.gsort_radix_workspace_bytes(n, 1) == HDR + state + 2 * keys
         ctiles = (n + 8191) // 8192
-        assert lib.gsort_compact_workspace_bytes(n) == HDR + -(-ctiles * 4 // 256) * 256
+        assert lib.gsort_compact_workspace_bytes(n) == HDR + up(ctiles * 128)   # a line per tile
     assert lib.gsort_radix_workspace_bytes(-1, 0) == 0
     assert lib.gsort_radix_workspace_bytes(1 << 30, 0) == 0
     assert lib.gsort_compact_workspace_bytes(1 << 30) == 0
