@@ -167,6 +167,25 @@ __device__ __forceinline__ LaneConsts lane_consts(uint32_t lane) {
     return c;
 }
 
+// Ballot of (d & bit) != 0 over the warp.
+__device__ __forceinline__ uint32_t ballot_bit(uint32_t d, uint32_t bit) {
+    return __ballot_sync(kFullMask, (d & bit) != 0u);
+}
+
+// (a ^ b) & c in one three-input logic operation.
+__device__ __forceinline__ uint32_t xor_and(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0x28;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
+
+// Position of the highest set bit (x != 0).
+__device__ __forceinline__ uint32_t highest_bit(uint32_t x) {
+    uint32_t r;
+    asm("bfind.u32 %0, %1;" : "=r"(r) : "r"(x));
+    return r;
+}
+
 template <int MATCH>
 __device__ __forceinline__ uint32_t digit_peers(uint32_t d, const LaneConsts &c) {
     if constexpr (MATCH == kMatchAny) {
@@ -183,11 +202,19 @@ __device__ __forceinline__ uint32_t digit_peers(uint32_t d, const LaneConsts &c)
     } else {
         uint32_t m[8];
 #pragma unroll
-        for (int b = 0; b < 8; ++b) m[b] = __ballot_sync(kFullMask, (d >> b) & 1u);
-        const uint32_t lo = (m[0] ^ c.inv[0]) & (m[1] ^ c.inv[1]) & (m[2] ^ c.inv[2]) &
-                            (m[3] ^ c.inv[3]) & (m[4] ^ c.inv[4]);
-        const uint32_t hi = (m[5] ^ c.inv[0]) & (m[6] ^ c.inv[1]) & (m[7] ^ c.inv[2]);
-        return __shfl_sync(kFullMask, lo, d & 31u) & __shfl_sync(kFullMask, hi, d >> 5);
+        for (int b = 0; b < 8; ++b) m[b] = ballot_bit(d, 1u << b);
+        // lo: lanes whose digit bits 0..4 equal this lane's id; hi: lanes whose
+        // digit bits 5..7 equal this lane's id bits 0..2
+        uint32_t lo = m[0] ^ c.inv[0];
+        lo = xor_and(m[1], c.inv[1], lo);
+        lo = xor_and(m[2], c.inv[2], lo);
+        lo = xor_and(m[3], c.inv[3], lo);
+        lo = xor_and(m[4], c.inv[4], lo);
+        uint32_t hi = m[5] ^ c.inv[0];
+        hi = xor_and(m[6], c.inv[1], hi);
+        hi = xor_and(m[7], c.inv[2], hi);
+        // a shuffle reads its source lane from the low five bits of its lane operand
+        return __shfl_sync(kFullMask, lo, d) & __shfl_sync(kFullMask, hi, d >> 5);
     }
 }
 
@@ -244,12 +271,19 @@ __device__ __forceinline__ bool look_back(const PassArgs &a, uint32_t tile, uint
 // global memory, or in a shared staging buffer); the tile-sorted keys/values
 // go to s_keys/s_vals (which may be the staging buffers: every key is in
 // registers before the first write).  tab = the shared tables: per-warp digit
-// counters, digit offsets, misc words.  Returns false when the tile stops
-// (device error or the test stall), after a block barrier.
-template <int WARPS, int IPT, int MATCH, int LW, bool BYTE, bool PAIRS, bool XIN, bool XOUT, bool FULL>
+// counters, digit offsets, misc words.  before_output() runs in every thread
+// after the last block barrier, before the output phase.  Returns false when
+// the tile stops (device error or the test stall), after that barrier.
+struct NoHook {
+    __device__ void operator()() const {}
+};
+
+template <int WARPS, int IPT, int MATCH, int LW, bool BYTE, bool PAIRS, bool XIN, bool XOUT, bool FULL,
+          class Hook = NoHook>
 __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, uint32_t tile,
                                           const uint32_t *kin, const uint32_t *vin,
-                                          uint32_t *s_keys, uint32_t *s_vals) {
+                                          uint32_t *s_keys, uint32_t *s_vals,
+                                          const Hook &before_output = Hook()) {
     constexpr int T = WARPS * 32;
     constexpr int TILE = T * IPT;
     uint32_t *s_cnt = tab;                      // [WARPS][256] counts, then next free slots
@@ -352,11 +386,11 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, uint
             const uint32_t d = valid ? digit_at<BYTE>(key[k], a.shift, a.mask) : 0u;
             uint32_t peers = digit_peers<MATCH>(d, c);
             if (!FULL) peers &= __ballot_sync(kFullMask, valid);
-            const int leader = 31 - __clz(peers);
+            const uint32_t leader = highest_bit(peers);   // peers is empty only for padding lanes
             uint32_t base = 0;
-            if (valid && lane == static_cast<uint32_t>(leader))
+            if (valid && lane == leader)
                 base = atomicAdd(&wc[d], static_cast<uint32_t>(__popc(peers)));
-            base = __shfl_sync(kFullMask, base, leader & 31);
+            base = __shfl_sync(kFullMask, base, leader);
             if (valid) {
                 const uint32_t slot = base + __popc(peers & ltm);
                 s_keys[slot] = key[k];
@@ -365,6 +399,7 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, uint
         }
     }
     __syncthreads();
+    before_output();
     if (s_misc[2] || tile == a.stall_tile) return false;
 
     // ---- contiguous runs per digit out to global memory
@@ -409,12 +444,13 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass(const PassArgs 
 }
 
 // ------------------------------------------------- persistent digit pass
-// A grid of (resident) CTAs loops over tiles.  While it processes tile k from
-// one shared buffer, the next tile it claimed is already on its way into the
-// other buffer through a TMA bulk copy, so neither the tile-id claim nor the
-// key loads wait on memory.  Tiles are still claimed in increasing order, and
-// each CTA processes its tiles in that order, so the smallest unfinished tile
-// can always complete: the look-back keeps making progress.
+// A grid of resident CTAs loops over tiles.  During the output phase of tile
+// k a CTA claims its next tile and starts a TMA bulk copy of its keys into the
+// other shared buffer, so the claim and the loads overlap the stores of tile
+// k.  A claimed tile waits only for one output phase before its counts are
+// published (claiming any earlier makes other tiles' look-backs wait), and
+// tiles are claimed and processed in increasing order, so the smallest
+// unfinished tile can always complete.
 constexpr uint32_t kBulkWaitLimit = 1u << 20;   // polls of a load barrier before giving up
 
 template <int WARPS, int IPT, bool PAIRS>
@@ -422,6 +458,38 @@ constexpr size_t persist_smem_words() {
     // 2 barriers (padded to 32 words), 2 key buffers [, 2 value buffers], tables
     return 32 + static_cast<size_t>(WARPS * 32 * IPT) * (PAIRS ? 4 : 2) + WARPS * kRow + 256 + 32;
 }
+
+template <int TILE, bool PAIRS>
+struct Prefetch {
+    const PassArgs *a;
+    uint64_t *bar;
+    uint32_t *kbuf, *vbuf;
+    // thread 0: bulk copy of tile t into buffer b
+    __device__ void operator()(uint32_t t, uint32_t b) const {
+        const uint32_t n_t = min(static_cast<uint32_t>(TILE), a->n - t * TILE);
+        const uint32_t bytes = (n_t & ~3u) * 4u;
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&bar[b], bytes * (PAIRS ? 2u : 1u));
+        if (bytes > 0) {
+            bulk_load(kbuf + b * TILE, a->src_k + t * TILE, bytes, &bar[b]);
+            if (PAIRS) bulk_load(vbuf + b * TILE, a->src_v + t * TILE, bytes, &bar[b]);
+        }
+    }
+};
+
+template <int TILE, bool PAIRS>
+struct ClaimNext {
+    const Prefetch<TILE, PAIRS> *pf;
+    uint32_t *counter, *slot;
+    uint32_t tiles, buffer;
+    __device__ void operator()() const {
+        if (threadIdx.x == 0) {
+            const uint32_t next = atomicAdd(counter, 1u);
+            *slot = next;
+            if (next < tiles) (*pf)(next, buffer);
+        }
+    }
+};
 
 template <int WARPS, int IPT, int MATCH, int LW, bool BYTE, bool PAIRS, bool XIN, bool XOUT>
 __global__ void __launch_bounds__(WARPS * 32, 2) k_digit_pass_persistent(const PassArgs a,
@@ -435,18 +503,7 @@ __global__ void __launch_bounds__(WARPS * 32, 2) k_digit_pass_persistent(const P
     uint32_t *tab = smem + 32 + static_cast<size_t>(TILE) * (PAIRS ? 4 : 2);
     uint32_t *s_misc = tab + WARPS * kRow + 256;
     const uint32_t tid = threadIdx.x;
-
-    // Issues the bulk copy of tile t into buffer b (thread 0 only).
-    auto prefetch = [&](uint32_t t, uint32_t b) {
-        const uint32_t n_t = min(static_cast<uint32_t>(TILE), a.n - t * TILE);
-        const uint32_t bytes = (n_t & ~3u) * 4u;
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(&bar[b], bytes * (PAIRS ? 2u : 1u));
-        if (bytes > 0) {
-            bulk_load(kbuf + b * TILE, a.src_k + t * TILE, bytes, &bar[b]);
-            if (PAIRS) bulk_load(vbuf + b * TILE, a.src_v + t * TILE, bytes, &bar[b]);
-        }
-    };
+    const Prefetch<TILE, PAIRS> prefetch{&a, bar, kbuf, vbuf};
 
     if (tid == 0) {
         mbar_init(&bar[0], 1);
@@ -460,13 +517,7 @@ __global__ void __launch_bounds__(WARPS * 32, 2) k_digit_pass_persistent(const P
     uint32_t b = 0;
     uint32_t phase[2] = {0u, 0u};
     while (tile < tiles) {
-        // claim the next tile and start its copy into the other buffer
-        if (tid == 0) {
-            const uint32_t next = atomicAdd(a.tile_counter, 1u);
-            s_misc[24] = next;
-            if (next < tiles) prefetch(next, b ^ 1u);
-            s_misc[2] = 0;
-        }
+        if (tid == 0) s_misc[2] = 0;
         for (uint32_t i = tid; i < WARPS * kRow; i += T) tab[i] = 0;
         const bool arrived = mbar_wait_bounded(&bar[b], phase[b], kBulkWaitLimit);
         const uint32_t tile_n = min(static_cast<uint32_t>(TILE), a.n - tile * TILE);
@@ -477,22 +528,21 @@ __global__ void __launch_bounds__(WARPS * 32, 2) k_digit_pass_persistent(const P
             kb[tile_n - rest + tid] = a.src_k[tile * TILE + tile_n - rest + tid];
             if (PAIRS) vb[tile_n - rest + tid] = a.src_v[tile * TILE + tile_n - rest + tid];
         }
-        const bool quit = __syncthreads_or(!arrived || (tid == 0 && ld_relaxed(a.abort_flag) != 0));
-        const uint32_t next = s_misc[24];
-        if (quit) {
+        if (__syncthreads_or(!arrived || (tid == 0 && ld_relaxed(a.abort_flag) != 0))) {
             // the result is void; leave only once no copy into this block is in flight
             if (tid == 0 && !arrived) record_error(a.status, a.abort_flag, GSORT_ETIMEOUT);
             if (!arrived) mbar_wait_bounded(&bar[b], phase[b], kBulkWaitLimit);
-            if (next < tiles) mbar_wait_bounded(&bar[b ^ 1u], phase[b ^ 1u], kBulkWaitLimit);
             return;
         }
         phase[b] ^= 1u;
+        const ClaimNext<TILE, PAIRS> claim{&prefetch, a.tile_counter, &s_misc[24], tiles, b ^ 1u};
         bool ok;
         if (tile_n == static_cast<uint32_t>(TILE))
-            ok = pass_tile<WARPS, IPT, MATCH, LW, BYTE, PAIRS, XIN, XOUT, true>(a, tab, tile, kb, vb, kb, vb);
+            ok = pass_tile<WARPS, IPT, MATCH, LW, BYTE, PAIRS, XIN, XOUT, true>(a, tab, tile, kb, vb, kb, vb, claim);
         else
-            ok = pass_tile<WARPS, IPT, MATCH, LW, BYTE, PAIRS, XIN, XOUT, false>(a, tab, tile, kb, vb, kb, vb);
-        __syncthreads();   // buffer b is read out before the next copy into it
+            ok = pass_tile<WARPS, IPT, MATCH, LW, BYTE, PAIRS, XIN, XOUT, false>(a, tab, tile, kb, vb, kb, vb, claim);
+        __syncthreads();   // buffer b is read out, and the next tile id is visible
+        const uint32_t next = s_misc[24];
         if (!ok && tile != a.stall_tile) {   // a look-back gave up
             if (next < tiles) mbar_wait_bounded(&bar[b ^ 1u], phase[b ^ 1u], kBulkWaitLimit);
             return;
@@ -603,16 +653,12 @@ struct Variant {
 };
 
 const Variant kVariants[] = {
-    {"one tile per CTA, 16 warps x 16 items, look-back window 8", PassConfig<16, 16, 2, kMatchTable, 8>::kTile,
-     &PassConfig<16, 16, 2, kMatchTable, 8>::launch},
+    {"one tile per CTA, 16 warps x 16 items", PassConfig<16, 16, 2, kMatchTable>::kTile,
+     &PassConfig<16, 16, 2, kMatchTable>::launch},
     {"persistent, 16 warps x 16 items, TMA prefetch", PersistentConfig<16, 16, kMatchTable>::kTile,
      &PersistentConfig<16, 16, kMatchTable>::launch},
     {"one tile per CTA, 8 warps x 16 items", PassConfig<8, 16, 3, kMatchTable>::kTile,
      &PassConfig<8, 16, 3, kMatchTable>::launch},
-    {"one tile per CTA, 16 warps x 16 items, look-back window 16", PassConfig<16, 16, 2, kMatchTable, 16>::kTile,
-     &PassConfig<16, 16, 2, kMatchTable, 16>::launch},
-    {"one tile per CTA, 16 warps x 16 items, look-back window 4", PassConfig<16, 16, 2, kMatchTable, 4>::kTile,
-     &PassConfig<16, 16, 2, kMatchTable, 4>::launch},
 };
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 
