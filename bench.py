@@ -123,6 +123,21 @@ class Clocks:
                 "samples": len(sm)}
 
 
+def reduce_max_ms(ms: float, dist, device) -> float:
+    """The slowest rank's time (every rank gets it); ms itself without a process group."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(ms_per_step: float, keys_per_rank: int, world: int) -> float:
+    """Whole-job Gkeys/s: the keys of all ranks over the slowest rank's step time."""
+    return world * keys_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
 def time_oracle_sort(keys: np.ndarray, min_seconds: float, max_reps: int):
     import oracle
     reps, t_total = 0, 0.0
@@ -254,13 +269,9 @@ def main():
     status = lib.gsort_check(ws.data_ptr(), stream.cuda_stream)
     if status != 0:
         raise RuntimeError(f"device-side error in the timed region: {status}")
-    ms_total = t_start.elapsed_time(t_end)
-    if dist is not None:
-        tt = torch.tensor([ms_total], dtype=torch.float64, device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = reduce_max_ms(t_start.elapsed_time(t_end), dist, device)
     ms_step = ms_total / args.steps
-    value = world * n / (ms_step * 1e-3) / 1e9
+    value = job_throughput(ms_step, n, world)
 
     pass_ms = [events[s][2 + p].elapsed_time(events[s][3 + p])
                for s in range(args.steps) for p in range(PASSES)]
