@@ -36,27 +36,82 @@ bool overlap(const void *a, const void *b, size_t bytes) { return ranges_overlap
 const gsort_options kDefaults = {0, -1, nullptr, 0, 0};
 
 int radix_args(const void *keys_in, void *keys_out, const uint32_t *vals_in, uint32_t *vals_out,
-               int64_t n, int kind, int begin_bit, int end_bit, const gsort_options *o) {
+               int64_t n, int kind, int flags, int begin_bit, int end_bit, const gsort_options *o) {
     if (n < 0) return GSORT_EINVAL;
     if (n > GSORT_MAX_N) return GSORT_ETOOBIG;
-    if (kind != GSORT_KEY_U32 && kind != GSORT_KEY_F32) return GSORT_EINVAL;
-    if (begin_bit < 0 || end_bit > 32 || begin_bit > end_bit) return GSORT_EINVAL;
+    const int kb = key_kind_bytes(kind);
+    if (kb == 0) return GSORT_EINVAL;
+    if ((flags & ~GSORT_DESCENDING) != 0) return GSORT_EINVAL;
+    if (begin_bit < 0 || end_bit > 8 * kb || begin_bit > end_bit) return GSORT_EINVAL;
     if ((vals_in == nullptr) != (vals_out == nullptr)) return GSORT_EINVAL;
-    if (o->variant < 0 || o->variant >= radix_num_variants()) return GSORT_EINVAL;
+    if (kb == 8 ? o->variant != 0 : (o->variant < 0 || o->variant >= radix_num_variants()))
+        return GSORT_EINVAL;
     if (o->num_events < 0 || (o->num_events > 0 && o->events == nullptr)) return GSORT_EINVAL;
     if (n == 0) return GSORT_OK;
     if (keys_in == nullptr || keys_out == nullptr) return GSORT_EINVAL;
-    if (!aligned(keys_in, 4) || !aligned(keys_out, 4)) return GSORT_EALIGN;
+    if (!aligned(keys_in, kb) || !aligned(keys_out, kb)) return GSORT_EALIGN;
     if (vals_in != nullptr && (!aligned(vals_in, 4) || !aligned(vals_out, 4))) return GSORT_EALIGN;
-    const size_t bytes = static_cast<size_t>(n) * 4;
-    if (partial_overlap(keys_in, keys_out, bytes)) return GSORT_EINVAL;
+    const size_t kbytes = static_cast<size_t>(n) * kb, vbytes = static_cast<size_t>(n) * 4;
+    if (partial_overlap(keys_in, keys_out, kbytes)) return GSORT_EINVAL;
     if (vals_in != nullptr) {
-        if (partial_overlap(vals_in, vals_out, bytes)) return GSORT_EINVAL;
-        if (overlap(keys_out, vals_out, bytes) || overlap(keys_in, vals_out, bytes) ||
-            overlap(keys_out, vals_in, bytes))
+        if (partial_overlap(vals_in, vals_out, vbytes)) return GSORT_EINVAL;
+        if (ranges_overlap(keys_out, kbytes, vals_out, vbytes) ||
+            ranges_overlap(keys_in, kbytes, vals_out, vbytes) ||
+            ranges_overlap(keys_out, kbytes, vals_in, vbytes))
             return GSORT_EINVAL;
     }
     return GSORT_OK;
+}
+
+int radix_sort(const void *d_keys_in, void *d_keys_out, const uint32_t *d_vals_in,
+               uint32_t *d_vals_out, int64_t n, int kind, int flags, int begin_bit, int end_bit,
+               void *d_ws, size_t ws_bytes, cudaStream_t stream, const gsort_options *options) {
+    const gsort_options *o = options ? options : &kDefaults;
+    int rc = radix_args(d_keys_in, d_keys_out, d_vals_in, d_vals_out, n, kind, flags, begin_bit,
+                        end_bit, o);
+    if (rc != GSORT_OK || n == 0) return rc;
+    const bool pairs = d_vals_in != nullptr;
+    const int kb = key_kind_bytes(kind);
+    if (d_ws == nullptr) return GSORT_EWORKSPACE;
+    if (!aligned(d_ws, kWsAlign)) return GSORT_EALIGN;
+    if (ws_bytes < radix_layout(static_cast<uint32_t>(n), pairs, kb).total) return GSORT_EWORKSPACE;
+    const size_t kbytes = static_cast<size_t>(n) * kb, vbytes = static_cast<size_t>(n) * 4;
+    if (ranges_overlap(d_ws, ws_bytes, d_keys_in, kbytes) ||
+        ranges_overlap(d_ws, ws_bytes, d_keys_out, kbytes) ||
+        (pairs && (ranges_overlap(d_ws, ws_bytes, d_vals_in, vbytes) ||
+                   ranges_overlap(d_ws, ws_bytes, d_vals_out, vbytes))))
+        return GSORT_EINVAL;
+    if (begin_bit == end_bit) {   // no key bits: the stable order is the input order
+        if (d_keys_out != d_keys_in &&
+            cudaMemcpyAsync(d_keys_out, d_keys_in, kbytes, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+            return GSORT_ECUDA;
+        if (pairs && d_vals_out != d_vals_in &&
+            cudaMemcpyAsync(d_vals_out, d_vals_in, vbytes, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+            return GSORT_ECUDA;
+        return GSORT_OK;
+    }
+    DeviceInfo dev;
+    if (device_info(&dev) != GSORT_OK) return GSORT_ECUDA;
+    RadixLaunch L;
+    L.keys_in = d_keys_in;
+    L.keys_out = d_keys_out;
+    L.vals_in = d_vals_in;
+    L.vals_out = d_vals_out;
+    L.n = static_cast<uint32_t>(n);
+    L.kind = kind;
+    L.flags = flags;
+    L.begin_bit = begin_bit;
+    L.end_bit = end_bit;
+    L.ws = static_cast<unsigned char *>(d_ws);
+    L.spin_limit = o->spin_limit ? o->spin_limit : kDefaultSpinLimit;
+    L.stall_tile = (o->stall_tile >= 0 && o->stall_tile < 0xFFFFFFFFll)
+                       ? static_cast<uint32_t>(o->stall_tile) : kNoStall;
+    L.events = reinterpret_cast<cudaEvent_t *>(o->events);
+    L.num_events = o->num_events;
+    L.variant = o->variant;
+    L.stream = stream;
+    L.sm_count = dev.sm_count;
+    return launch_radix(L);
 }
 
 }  // namespace
@@ -83,56 +138,37 @@ int gsort_version(void) { return 100; }
 
 size_t gsort_radix_workspace_bytes(int64_t n, int with_values) {
     if (n < 0 || n > GSORT_MAX_N) return 0;
-    return radix_layout(static_cast<uint32_t>(n), with_values != 0).total;
+    return radix_layout(static_cast<uint32_t>(n), with_values != 0, 4).total;
+}
+
+size_t gsort_radix_sort_workspace_bytes(int64_t n, int kind, int with_values) {
+    const int kb = key_kind_bytes(kind);
+    if (n < 0 || n > GSORT_MAX_N || kb == 0) return 0;
+    return radix_layout(static_cast<uint32_t>(n), with_values != 0, kb).total;
+}
+
+int gsort_radix_sort_ex(const void *d_keys_in, void *d_keys_out, const uint32_t *d_vals_in,
+                        uint32_t *d_vals_out, int64_t n, int kind, int flags, int begin_bit,
+                        int end_bit, void *d_ws, size_t ws_bytes, cudaStream_t stream,
+                        const gsort_options *options) {
+    return radix_sort(d_keys_in, d_keys_out, d_vals_in, d_vals_out, n, kind, flags, begin_bit,
+                      end_bit, d_ws, ws_bytes, stream, options);
+}
+
+int gsort_radix_sort(const void *d_keys_in, void *d_keys_out, const uint32_t *d_vals_in,
+                     uint32_t *d_vals_out, int64_t n, int kind, int flags, int begin_bit,
+                     int end_bit, void *d_ws, size_t ws_bytes, cudaStream_t stream) {
+    return radix_sort(d_keys_in, d_keys_out, d_vals_in, d_vals_out, n, kind, flags, begin_bit,
+                      end_bit, d_ws, ws_bytes, stream, nullptr);
 }
 
 int gsort_radix_pairs_ex(const void *d_keys_in, void *d_keys_out, const uint32_t *d_vals_in,
                          uint32_t *d_vals_out, int64_t n, int kind, int begin_bit, int end_bit,
                          void *d_ws, size_t ws_bytes, cudaStream_t stream,
                          const gsort_options *options) {
-    const gsort_options *o = options ? options : &kDefaults;
-    int rc = radix_args(d_keys_in, d_keys_out, d_vals_in, d_vals_out, n, kind, begin_bit, end_bit, o);
-    if (rc != GSORT_OK || n == 0) return rc;
-    const bool pairs = d_vals_in != nullptr;
-    if (d_ws == nullptr) return GSORT_EWORKSPACE;
-    if (!aligned(d_ws, kWsAlign)) return GSORT_EALIGN;
-    if (ws_bytes < radix_layout(static_cast<uint32_t>(n), pairs).total) return GSORT_EWORKSPACE;
-    const size_t bytes = static_cast<size_t>(n) * 4;
-    if (ranges_overlap(d_ws, ws_bytes, d_keys_in, bytes) ||
-        ranges_overlap(d_ws, ws_bytes, d_keys_out, bytes) ||
-        (pairs && (ranges_overlap(d_ws, ws_bytes, d_vals_in, bytes) ||
-                   ranges_overlap(d_ws, ws_bytes, d_vals_out, bytes))))
-        return GSORT_EINVAL;
-    if (begin_bit == end_bit) {   // no key bits: the stable order is the input order
-        if (d_keys_out != d_keys_in &&
-            cudaMemcpyAsync(d_keys_out, d_keys_in, bytes, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
-            return GSORT_ECUDA;
-        if (pairs && d_vals_out != d_vals_in &&
-            cudaMemcpyAsync(d_vals_out, d_vals_in, bytes, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
-            return GSORT_ECUDA;
-        return GSORT_OK;
-    }
-    DeviceInfo dev;
-    if (device_info(&dev) != GSORT_OK) return GSORT_ECUDA;
-    RadixLaunch L;
-    L.keys_in = static_cast<const uint32_t *>(d_keys_in);
-    L.keys_out = static_cast<uint32_t *>(d_keys_out);
-    L.vals_in = d_vals_in;
-    L.vals_out = d_vals_out;
-    L.n = static_cast<uint32_t>(n);
-    L.kind = kind;
-    L.begin_bit = begin_bit;
-    L.end_bit = end_bit;
-    L.ws = static_cast<unsigned char *>(d_ws);
-    L.spin_limit = o->spin_limit ? o->spin_limit : kDefaultSpinLimit;
-    L.stall_tile = (o->stall_tile >= 0 && o->stall_tile < 0xFFFFFFFFll)
-                       ? static_cast<uint32_t>(o->stall_tile) : kNoStall;
-    L.events = reinterpret_cast<cudaEvent_t *>(o->events);
-    L.num_events = o->num_events;
-    L.variant = o->variant;
-    L.stream = stream;
-    L.sm_count = dev.sm_count;
-    return launch_radix(L);
+    if (key_kind_bytes(kind) != 4) return GSORT_EINVAL;   // 64-bit kinds: gsort_radix_sort
+    return radix_sort(d_keys_in, d_keys_out, d_vals_in, d_vals_out, n, kind, 0, begin_bit, end_bit,
+                      d_ws, ws_bytes, stream, options);
 }
 
 int gsort_radix_pairs(const void *d_keys_in, void *d_keys_out, const uint32_t *d_vals_in,
@@ -152,19 +188,20 @@ int gsort_digit_histograms(const void *d_keys, int64_t n, int kind, int begin_bi
                            uint32_t *d_hist_out, cudaStream_t stream) {
     if (n < 0) return GSORT_EINVAL;
     if (n > GSORT_MAX_N) return GSORT_ETOOBIG;
-    if (kind != GSORT_KEY_U32 && kind != GSORT_KEY_F32) return GSORT_EINVAL;
-    if (begin_bit < 0 || end_bit > 32 || begin_bit > end_bit) return GSORT_EINVAL;
+    const int kb = key_kind_bytes(kind);
+    if (kb == 0) return GSORT_EINVAL;
+    if (begin_bit < 0 || end_bit > 8 * kb || begin_bit > end_bit) return GSORT_EINVAL;
     if (begin_bit == end_bit) return GSORT_OK;
     if (d_hist_out == nullptr || (n > 0 && d_keys == nullptr)) return GSORT_EINVAL;
-    if (!aligned(d_hist_out, 4) || (n > 0 && !aligned(d_keys, 4))) return GSORT_EALIGN;
+    if (!aligned(d_hist_out, 4) || (n > 0 && !aligned(d_keys, kb))) return GSORT_EALIGN;
     const int passes = (end_bit - begin_bit + 7) / 8;
-    if (n > 0 && ranges_overlap(d_keys, static_cast<size_t>(n) * 4, d_hist_out,
+    if (n > 0 && ranges_overlap(d_keys, static_cast<size_t>(n) * kb, d_hist_out,
                                 static_cast<size_t>(passes) * 256 * 4))
         return GSORT_EINVAL;
     DeviceInfo dev;
     if (device_info(&dev) != GSORT_OK) return GSORT_ECUDA;
-    return launch_digit_histograms(static_cast<const uint32_t *>(d_keys), static_cast<uint32_t>(n),
-                                   kind, begin_bit, end_bit, d_hist_out, stream, dev.sm_count);
+    return launch_digit_histograms(d_keys, static_cast<uint32_t>(n), kind, 0, begin_bit, end_bit,
+                                   d_hist_out, stream, dev.sm_count);
 }
 
 size_t gsort_compact_workspace_bytes(int64_t n) {
@@ -246,9 +283,14 @@ int gsort_radix_num_variants(void) { return radix_num_variants(); }
 const char *gsort_radix_variant_name(int variant) { return radix_variant_name(variant); }
 
 int gsort_radix_launch_count(int64_t n, int begin_bit, int end_bit, int in_place) {
-    if (n <= 0 || begin_bit >= end_bit) return 0;
+    return gsort_radix_sort_launch_count(n, GSORT_KEY_U32, begin_bit, end_bit, in_place);
+}
+
+int gsort_radix_sort_launch_count(int64_t n, int kind, int begin_bit, int end_bit, int in_place) {
+    const int kb = key_kind_bytes(kind);
+    if (n <= 0 || begin_bit >= end_bit || kb == 0) return 0;
     const int passes = (end_bit - begin_bit + 7) / 8;
-    return 2 + passes + ((in_place && (passes & 1)) ? 1 : 0);
+    return 2 + passes + ((in_place && (passes & 1)) ? 1 : 0) + (kb == 8 ? 1 : 0);
 }
 
 }  // extern "C"

@@ -18,7 +18,7 @@ constexpr size_t kHdrAbort = 4;       // u32: non-zero once a wait gave up; late
 constexpr size_t kHdrCounters = 128;  // u32 tile counters, one per 128-byte line
 constexpr int kNumCounters = 8;
 constexpr size_t kHdrKept = kHdrCounters + 128 * kNumCounters;  // u64 kept count (compaction)
-constexpr size_t kHdrHist = 2048;     // u32[4][256] digit histograms (radix)
+constexpr size_t kHdrHist = 2048;     // u32[4][256] digit histograms (radix, 32-bit keys)
 constexpr size_t kHdrBytes = 8192;    // header size, keeps what follows 256-byte aligned
 constexpr size_t kWsAlign = 256;
 
@@ -67,18 +67,6 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     uint32_t m;
     asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
     return m;
-}
-
-// Order-preserving map of float bit patterns to unsigned integers: negative
-// values have every bit flipped, non-negative values only the sign bit
-// ([PMPP10] section 8, exercise 7; IEEE totalOrder for non-NaN values).
-__device__ __forceinline__ uint32_t float_key_in(uint32_t bits) {
-    return bits ^ (static_cast<uint32_t>(static_cast<int32_t>(bits) >> 31) | 0x80000000u);
-}
-
-// Inverse of float_key_in.
-__device__ __forceinline__ uint32_t float_key_out(uint32_t u) {
-    return u ^ (((u >> 31) - 1u) | 0x80000000u);
 }
 
 // Inclusive warp scan (Kogge-Stone over shuffles).
@@ -166,13 +154,32 @@ int device_info(DeviceInfo *out);  // returns GSORT_OK or GSORT_ECUDA
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // ------------------------------------------------------------ launch plans
+// Order map of a key kind and direction: ordered = (float ? float_map(bits)
+// : bits) ^ flip, on key words of key_bytes bytes.
+struct KeyOrder {
+    int key_bytes;
+    uint64_t fmask;   // all ones for float kinds, else 0
+    uint64_t flip;    // sign bit for signed kinds, complemented for descending order
+};
+KeyOrder key_order(int kind, int flags);
+
+// Bytes of one key of `kind` (4 or 8), 0 for an unknown kind.
+inline int key_kind_bytes(int kind) {
+    switch (kind) {
+        case GSORT_KEY_U32: case GSORT_KEY_F32: case GSORT_KEY_I32: return 4;
+        case GSORT_KEY_U64: case GSORT_KEY_F64: case GSORT_KEY_I64: return 8;
+        default: return 0;
+    }
+}
+
 struct RadixLaunch {
-    const uint32_t *keys_in;
-    uint32_t *keys_out;
+    const void *keys_in;
+    void *keys_out;
     const uint32_t *vals_in;  // null: keys only
     uint32_t *vals_out;
     uint32_t n;
     int kind;
+    int flags;
     int begin_bit, end_bit;
     unsigned char *ws;
     uint32_t spin_limit;
@@ -187,11 +194,12 @@ struct RadixLaunch {
 // Layout of the radix workspace after the header.
 struct RadixLayout {
     uint32_t tiles_max;   // tiles of the smallest tile size any variant uses
+    size_t hist;          // u32[passes][256] digit histograms
     size_t look_a, look_b;  // [tiles_max][256] look-back words, alternating between passes
     size_t tmp_keys, tmp_vals;
     size_t total;
 };
-RadixLayout radix_layout(uint32_t n, bool with_values);
+RadixLayout radix_layout(uint32_t n, bool with_values, int key_bytes);
 
 int radix_num_variants();
 const char *radix_variant_name(int v);
@@ -199,7 +207,7 @@ uint32_t radix_variant_tile(int v);
 
 // Launchers (each returns GSORT_OK or GSORT_ECUDA).
 int launch_radix(const RadixLaunch &L);
-int launch_digit_histograms(const uint32_t *keys, uint32_t n, int kind, int begin_bit,
+int launch_digit_histograms(const void *keys, uint32_t n, int kind, int flags, int begin_bit,
                             int end_bit, uint32_t *hist_out, cudaStream_t stream, int sm_count);
 
 struct CompactLayout {

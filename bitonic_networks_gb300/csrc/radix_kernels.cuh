@@ -1,0 +1,604 @@
+// radix_kernels.cuh -- device code of the LSD radix sort, generic in the key
+// word (32- or 64-bit), shared by radix.cu (32-bit keys) and radix64.cu
+// (64-bit keys).
+//
+// Steps (page tags as in include/gsort.h):
+//   histogram  one read of the keys builds the 256-bin histogram of every
+//              digit pass ([CUDA3] "processing several bits at once", kernel 1;
+//              [PMPP10] 10.3 histogram step) and clears the first pass's
+//              look-back words
+//   P x pass   single-pass digit scatter ([CUDA3] kernel 3): each tile ranks
+//              its keys stably per digit with a warp multisplit, publishes its
+//              per-digit counts, looks back over earlier tiles' counts
+//              (decoupled look-back), and writes every key to
+//                bin start of its digit (exclusive scan of the pass histogram,
+//                [CUDA3] kernel 2, done per tile from the 256 counts)
+//              + count of the digit in earlier tiles
+//              + stable rank of the key among the tile's keys of that digit,
+//              after reordering the tile in shared memory so that global
+//              writes go out as contiguous runs per digit ([PMPP10] 10.4 data
+//              buffering).  Values move with their keys ([PMPP10] 10.6).
+//
+// Key kinds other than unsigned ascending are sorted through an order map
+// applied when a pass first loads a key and inverted when the last pass
+// stores it: floats ([PMPP10] section 8, exercise 7) map to unsigned integers
+// in IEEE totalOrder, signed integers flip their sign bit (the same idea for
+// two's complement), and descending order ([PMPP10] section 8, exercise 6)
+// complements the mapped key, which keeps equal keys in input order.
+// Intermediate passes move the mapped keys.  64-bit keys take 8 passes of
+// radix 256 ([PMPP10] section 8, exercise 2).
+//
+// Differences from the pages' kernels: the in-tile rank comes from a warp
+// multisplit (peer mask of equal digits + popcount below the lane) instead of
+// eight block-wide 1-bit splits; a tile counts its digits first (cheap shared
+// atomics) and publishes the counts before ranking, so its look-back overlaps
+// other warps' ranking, and the per-warp counters then hand out tile slots
+// directly; look-back words are cleared one row per tile by the previous
+// kernel instead of a memset per pass; every wait is bounded.
+#pragma once
+
+#include <algorithm>
+#include <type_traits>
+
+#include "gsort_internal.cuh"
+
+namespace gsort {
+
+// Arguments of one digit pass.  Key arrays hold 32- or 64-bit words (the
+// kernel's key type); values are 32-bit.
+struct PassArgs {
+    const void *src_k;
+    void *dst_k;
+    const uint32_t *src_v;
+    uint32_t *dst_v;
+    uint32_t n;
+    uint32_t shift;         // digit = (key >> shift) & mask
+    uint32_t mask;
+    uint64_t fmask;         // order map: all ones for float keys, else 0
+    uint64_t flip;          // order map: bits flipped after the float map
+    const uint32_t *hist;   // the 256 counts of this pass
+    uint32_t *look;         // [tiles][256] look-back words of this pass (cleared): flag | count
+    uint32_t *look_clear;   // next pass's words: row `tile` is cleared here; may be null
+    uint32_t *tile_counter;
+    uint32_t *status;
+    uint32_t *abort_flag;
+    uint32_t spin_limit;
+    uint32_t stall_tile;
+};
+
+// Launch of one digit pass over `tiles` tiles (one configuration of the kernel).
+using PassLauncher = cudaError_t (*)(const PassArgs &, bool pairs, bool xin, bool xout,
+                                     uint32_t tiles, cudaStream_t);
+
+// 64-bit keys (radix64.cu): the digit pass, its tile size, and the histogram.
+cudaError_t launch_pass_u64(const PassArgs &a, bool pairs, bool xin, bool xout, uint32_t tiles,
+                            cudaStream_t s);
+uint32_t pass_tile_u64();
+cudaError_t launch_hist_u64(const uint64_t *keys, uint32_t n, bool xf, uint64_t fmask, uint64_t flip,
+                            int begin_bit, int passes, uint32_t last_mask, uint32_t *hist,
+                            uint32_t *clear, uint32_t clear_words, cudaStream_t s, int sm_count);
+
+namespace {
+
+// ------------------------------------------------------------- order map
+// ordered = (float ? float_map(bits) : bits) ^ flip, where float_map flips
+// every bit of a negative value and only the sign bit of a non-negative one.
+template <class K>
+__device__ __forceinline__ K order_in(K bits, K fmask, K flip) {
+    using S = typename std::conditional<sizeof(K) == 8, int64_t, int32_t>::type;
+    constexpr K sign = K(1) << (8 * sizeof(K) - 1);
+    const K m = static_cast<K>(static_cast<S>(bits) >> (8 * sizeof(K) - 1)) | sign;
+    return bits ^ (m & fmask) ^ flip;
+}
+
+// Inverse of order_in.
+template <class K>
+__device__ __forceinline__ K order_out(K u, K fmask, K flip) {
+    using S = typename std::conditional<sizeof(K) == 8, int64_t, int32_t>::type;
+    constexpr K sign = K(1) << (8 * sizeof(K) - 1);
+    const K y = u ^ flip;
+    const K m = static_cast<K>(static_cast<S>(~y) >> (8 * sizeof(K) - 1)) | sign;
+    return y ^ (m & fmask);
+}
+
+// Digit of key k at bit `shift`.  BYTE: the digit is a whole byte of the key
+// (shift a multiple of 8, full 8-bit mask), extracted with one byte permute.
+template <bool BYTE>
+__device__ __forceinline__ uint32_t digit_at(uint32_t k, uint32_t shift, uint32_t mask) {
+    if constexpr (BYTE) return __byte_perm(k, 0u, 0x4440u | (shift >> 3));
+    else return (k >> shift) & mask;
+}
+
+template <bool BYTE>
+__device__ __forceinline__ uint32_t digit_at(uint64_t k, uint32_t shift, uint32_t mask) {
+    if constexpr (BYTE) {
+        const uint32_t w = (shift & 32u) ? static_cast<uint32_t>(k >> 32) : static_cast<uint32_t>(k);
+        return __byte_perm(w, 0u, 0x4440u | ((shift & 31u) >> 3));
+    } else {
+        return static_cast<uint32_t>(k >> shift) & mask;
+    }
+}
+
+// -------------------------------------------------------------- init
+__global__ void k_zero_words(uint32_t *p, uint32_t nwords) {
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < nwords;
+         i += gridDim.x * blockDim.x)
+        p[i] = 0;
+}
+
+// -------------------------------------------------------------- histogram
+// Every lane owns a private column of counters, so the shared-memory atomics
+// of a warp never conflict, whatever the keys (equal keys included).  One
+// 1024-thread CTA per SM; the columns are summed once per CTA and added to
+// the global histogram.
+//   32-bit keys: counter (pass, digit, lane) at word ((pass*256 + digit)*32 +
+//                lane), up to 4 passes: 128 KiB.
+//   64-bit keys: 16-bit counters, two digits per word: (pass, digit) in half
+//                (digit & 1) of word ((pass*128 + digit/2)*32 + lane), up to 8
+//                passes: 128 KiB.  A lane counts at most ceil(n / (grid *
+//                1024)) keys, far below 2^16 for n <= 2^30 and the grid below.
+constexpr int kHistThreads = 1024;
+constexpr int kHistUnroll = 4;    // 16-byte loads in flight per thread
+constexpr size_t kHistSmemBytes = 4 * 256 * 32 * sizeof(uint32_t);
+
+template <bool XF, bool BYTE>
+__device__ __forceinline__ void hist_count(uint32_t *col, uint32_t k, uint32_t begin_bit,
+                                           int passes, uint32_t last_mask, uint32_t fmask,
+                                           uint32_t flip) {
+    if (XF) k = order_in<uint32_t>(k, fmask, flip);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        if (p < passes) {
+            const uint32_t d = digit_at<BYTE>(k, begin_bit + 8 * p, p == passes - 1 ? last_mask : 0xFFu);
+            atomicAdd(&col[(p * 256 + d) * 32], 1u);
+        }
+    }
+}
+
+template <bool XF, bool BYTE>
+__device__ __forceinline__ void hist_count(uint32_t *col, uint64_t k, uint32_t begin_bit,
+                                           int passes, uint32_t last_mask, uint64_t fmask,
+                                           uint64_t flip) {
+    if (XF) k = order_in<uint64_t>(k, fmask, flip);
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        if (p < passes) {
+            const uint32_t d = digit_at<BYTE>(k, begin_bit + 8 * p, p == passes - 1 ? last_mask : 0xFFu);
+            atomicAdd(&col[(p * 128 + (d >> 1)) * 32], 1u << ((d & 1u) * 16u));
+        }
+    }
+}
+
+template <class K, bool XF, bool BYTE>
+__global__ void __launch_bounds__(kHistThreads, 1)
+k_digit_hist(const K *__restrict__ keys, uint32_t n, uint32_t begin_bit, int passes,
+             uint32_t last_mask, K fmask, K flip, uint32_t *__restrict__ hist,
+             uint4 *__restrict__ clear, uint32_t clear_vec4) {
+    constexpr bool kWide = sizeof(K) == 8;
+    constexpr uint32_t kPerVec = 16 / sizeof(K);   // keys per 16-byte load
+    extern __shared__ uint32_t s_h[];
+    const uint32_t tid = threadIdx.x;
+    const uint32_t words = static_cast<uint32_t>(passes) * (kWide ? 128 : 256) * 32;
+    for (uint32_t i = tid; i < words; i += kHistThreads) s_h[i] = 0;
+    const uint32_t gtid = blockIdx.x * kHistThreads + tid;
+    const uint32_t gstride = gridDim.x * kHistThreads;
+    for (uint32_t i = gtid; i < clear_vec4; i += gstride) clear[i] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+
+    uint32_t *col = s_h + (tid & 31);
+    // elements before the first 16-byte boundary, the vector body, the tail
+    uint32_t head = static_cast<uint32_t>(((16 - (reinterpret_cast<uintptr_t>(keys) & 15)) & 15) / sizeof(K));
+    head = min(head, n);
+    const uint32_t nvec = (n - head) / kPerVec;
+    const uint4 *vec = reinterpret_cast<const uint4 *>(keys + head);
+    for (uint32_t v = gtid; v < nvec; v += kHistUnroll * gstride) {
+        uint4 q[kHistUnroll];
+#pragma unroll
+        for (int u = 0; u < kHistUnroll; ++u) {
+            const uint32_t idx = v + u * gstride;
+            if (idx < nvec) q[u] = __ldcs(vec + idx);
+        }
+#pragma unroll
+        for (int u = 0; u < kHistUnroll; ++u) {
+            if (v + u * gstride < nvec) {
+                if constexpr (kWide) {
+                    const uint64_t a = (static_cast<uint64_t>(q[u].y) << 32) | q[u].x;
+                    const uint64_t b = (static_cast<uint64_t>(q[u].w) << 32) | q[u].z;
+                    hist_count<XF, BYTE>(col, a, begin_bit, passes, last_mask, fmask, flip);
+                    hist_count<XF, BYTE>(col, b, begin_bit, passes, last_mask, fmask, flip);
+                } else {
+                    hist_count<XF, BYTE>(col, q[u].x, begin_bit, passes, last_mask, fmask, flip);
+                    hist_count<XF, BYTE>(col, q[u].y, begin_bit, passes, last_mask, fmask, flip);
+                    hist_count<XF, BYTE>(col, q[u].z, begin_bit, passes, last_mask, fmask, flip);
+                    hist_count<XF, BYTE>(col, q[u].w, begin_bit, passes, last_mask, fmask, flip);
+                }
+            }
+        }
+    }
+    const uint32_t tail0 = head + nvec * kPerVec;
+    if (gtid < head) hist_count<XF, BYTE>(col, keys[gtid], begin_bit, passes, last_mask, fmask, flip);
+    if (gtid < n - tail0)
+        hist_count<XF, BYTE>(col, keys[tail0 + gtid], begin_bit, passes, last_mask, fmask, flip);
+    __syncthreads();
+
+    // sum each (pass, digit) row over the 32 lane columns; the rotated start
+    // keeps the 32 threads of a warp on 32 different banks
+    for (uint32_t i = tid; i < static_cast<uint32_t>(passes) * 256; i += kHistThreads) {
+        uint32_t s = 0;
+        if constexpr (kWide) {
+            const uint32_t row = (i >> 8) * 128 + ((i & 255u) >> 1), half = (i & 1u) * 16u;
+#pragma unroll 8
+            for (uint32_t j = 0; j < 32; ++j) s += (s_h[row * 32 + ((j + row) & 31)] >> half) & 0xFFFFu;
+        } else {
+#pragma unroll 8
+            for (uint32_t j = 0; j < 32; ++j) s += s_h[i * 32 + ((j + i) & 31)];
+        }
+        if (s) atomicAdd(&hist[i], s);
+    }
+}
+
+// ------------------------------------------------------- warp multisplit
+// Ranking methods for the mask of lanes whose digit equals this lane's:
+//   kMatchTable  the eight ballots (bit planes of the warp's digits) are turned
+//                into two lane-distributed tables: lane l holds the mask of
+//                lanes whose low five digit bits equal l, and the mask of lanes
+//                whose top three bits equal l & 7 (built with per-lane
+//                constants, no per-key bit tests); a lane fetches its two
+//                entries with two shuffles and ANDs them.
+//   kMatchSelect each lane selects, per bit, the ballot or its complement.
+//   kMatchAny    the hardware match.any instruction.
+constexpr int kMatchTable = 0, kMatchSelect = 1, kMatchAny = 2;
+
+struct LaneConsts {
+    uint32_t inv[5];   // ~0 where bit b of the lane id is 0, else 0
+};
+
+__device__ __forceinline__ LaneConsts lane_consts(uint32_t lane) {
+    LaneConsts c;
+#pragma unroll
+    for (int b = 0; b < 5; ++b) c.inv[b] = ((lane >> b) & 1u) ? 0u : kFullMask;
+    return c;
+}
+
+// Ballot of (d & bit) != 0 over the warp.
+__device__ __forceinline__ uint32_t ballot_bit(uint32_t d, uint32_t bit) {
+    return __ballot_sync(kFullMask, (d & bit) != 0u);
+}
+
+// (a ^ b) & c in one three-input logic operation.
+__device__ __forceinline__ uint32_t xor_and(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0x28;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
+
+// Position of the highest set bit (x != 0).
+__device__ __forceinline__ uint32_t highest_bit(uint32_t x) {
+    uint32_t r;
+    asm("bfind.u32 %0, %1;" : "=r"(r) : "r"(x));
+    return r;
+}
+
+template <int MATCH>
+__device__ __forceinline__ uint32_t digit_peers(uint32_t d, const LaneConsts &c) {
+    if constexpr (MATCH == kMatchAny) {
+        return __match_any_sync(kFullMask, d);
+    } else if constexpr (MATCH == kMatchSelect) {
+        uint32_t peers = kFullMask;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const bool bit = (d >> b) & 1u;
+            const uint32_t m = __ballot_sync(kFullMask, bit);
+            peers &= bit ? m : ~m;
+        }
+        return peers;
+    } else {
+        uint32_t m[8];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) m[b] = ballot_bit(d, 1u << b);
+        // lo: lanes whose digit bits 0..4 equal this lane's id; hi: lanes whose
+        // digit bits 5..7 equal this lane's id bits 0..2
+        uint32_t lo = m[0] ^ c.inv[0];
+        lo = xor_and(m[1], c.inv[1], lo);
+        lo = xor_and(m[2], c.inv[2], lo);
+        lo = xor_and(m[3], c.inv[3], lo);
+        lo = xor_and(m[4], c.inv[4], lo);
+        uint32_t hi = m[5] ^ c.inv[0];
+        hi = xor_and(m[6], c.inv[1], hi);
+        hi = xor_and(m[7], c.inv[2], hi);
+        // a shuffle reads its source lane from the low five bits of its lane operand
+        return __shfl_sync(kFullMask, lo, d) & __shfl_sync(kFullMask, hi, d >> 5);
+    }
+}
+
+constexpr int kRow = 256;   // per-warp digit counters
+
+template <class K, int WARPS, int IPT, bool PAIRS>
+__host__ __device__ constexpr size_t pass_smem_words() {
+    // keys [+ values] of the tile, per-warp counters, 256 digit offsets, 32 misc words
+    return static_cast<size_t>(WARPS * 32 * IPT) * (sizeof(K) / 4 + (PAIRS ? 1 : 0)) + WARPS * kRow +
+           256 + 32;
+}
+
+// Exclusive prefix of digit d over all tiles before `tile`.  Each word holds a
+// flag (AGG: the tile's count; PREFIX: the count over tiles 0..t) and a
+// 30-bit count, so one round trip reads W predecessors at once; the
+// nearest PREFIX word ends the walk and the AGG words before it are summed.
+// Returns false if a wait gave up.
+template <int W>
+__device__ __forceinline__ bool look_back(const PassArgs &a, uint32_t tile, uint32_t d,
+                                          uint32_t &excl) {
+    excl = 0;
+    int32_t t = static_cast<int32_t>(tile) - 1;
+    uint32_t polls = 0, ns = 32;
+    while (true) {
+        uint32_t w[W];
+#pragma unroll
+        for (int i = 0; i < W; ++i)
+            w[i] = (t - i >= 0) ? ld_relaxed(a.look + static_cast<uint32_t>(t - i) * 256 + d)
+                                : kFlagPrefix;   // before tile 0: an empty prefix
+        // sum words up to and including the nearest PREFIX; any empty word
+        // before it means a predecessor has not published yet
+        uint32_t sum = 0;
+        bool done = false, pending = false;
+#pragma unroll
+        for (int i = 0; i < W; ++i) {
+            if (!done) {
+                pending |= (w[i] & ~kValueMask) == 0;
+                sum += w[i] & kValueMask;
+                done = (w[i] & kFlagPrefix) != 0;
+            }
+        }
+        if (pending) {
+            if (++polls >= a.spin_limit || ld_relaxed(a.abort_flag)) return false;
+            backoff(ns);
+            continue;
+        }
+        excl += sum;
+        if (done) return true;
+        t -= W;
+    }
+}
+
+// One tile of a digit pass.  kin/vin point at the tile's first key/value (in
+// global memory, or in a shared staging buffer); the tile-sorted keys/values
+// go to s_keys/s_vals (which may be the staging buffers: every key is in
+// registers before the first write).  tab = the shared tables: per-warp digit
+// counters, digit offsets, misc words.  before_output() runs in every thread
+// after the last block barrier, before the output phase.  Returns false when
+// the tile stops (device error or the test stall), after that barrier.
+struct NoHook {
+    __device__ void operator()() const {}
+};
+
+template <class K, int WARPS, int IPT, int MATCH, int LW, bool BYTE, bool PAIRS, bool XIN, bool XOUT,
+          bool FULL, class Hook = NoHook>
+__device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, uint32_t tile,
+                                          const K *kin, const uint32_t *vin,
+                                          K *s_keys, uint32_t *s_vals,
+                                          const Hook &before_output = Hook()) {
+    constexpr int T = WARPS * 32;
+    constexpr int TILE = T * IPT;
+    uint32_t *s_cnt = tab;                      // [WARPS][256] counts, then next free slots
+    uint32_t *s_goff = s_cnt + WARPS * kRow;    // [256] global index - tile slot
+    uint32_t *s_misc = s_goff + 256;            // [32]
+
+    const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t tile_base = tile * TILE;
+    const uint32_t tile_n = FULL ? TILE : a.n - tile_base;
+    // Item k of this thread sits at tile index item0 + 32k: each warp owns a
+    // contiguous run of 32*IPT keys and walks it in order, which makes the
+    // warp-local ranks stable.
+    const uint32_t item0 = warp * (32 * IPT) + lane;
+    K key[IPT];
+#pragma unroll
+    for (int k = 0; k < IPT; ++k) {
+        const uint32_t i = item0 + k * 32;
+        key[k] = (FULL || i < tile_n) ? kin[i] : K(0);
+        if (XIN) key[k] = order_in<K>(key[k], static_cast<K>(a.fmask), static_cast<K>(a.flip));
+    }
+    uint32_t val[PAIRS ? IPT : 1];
+    if (PAIRS) {
+#pragma unroll
+        for (int k = 0; k < IPT; ++k) {
+            const uint32_t i = item0 + k * 32;
+            val[k] = (FULL || i < tile_n) ? vin[i] : 0u;
+        }
+    }
+
+    // ---- early counts: this warp's keys per digit (order does not matter here)
+    {
+        uint32_t *wc = s_cnt + warp * kRow;
+#pragma unroll
+        for (int k = 0; k < IPT; ++k)
+            if (FULL || item0 + k * 32 < tile_n) atomicAdd(&wc[digit_at<BYTE>(key[k], a.shift, a.mask)], 1u);
+    }
+    __syncthreads();
+
+    // ---- tile counts per digit, published at once; scans over the 256 digits
+    uint32_t cnt = 0, tile_excl = 0, bin_excl = 0;
+    if (tid < 256) {
+#pragma unroll
+        for (int w = 0; w < WARPS; ++w) {
+            const uint32_t cw = s_cnt[w * kRow + tid];
+            s_cnt[w * kRow + tid] = cnt;   // exclusive over warps
+            cnt += cw;
+        }
+        if (tile != a.stall_tile)
+            st_relaxed(a.look + tile * 256 + tid, (tile == 0 ? kFlagPrefix : kFlagAgg) | cnt);
+        const uint32_t bin = a.hist[tid];
+        const uint32_t ic = warp_inclusive_scan(cnt, lane);
+        const uint32_t ib = warp_inclusive_scan(bin, lane);
+        if (lane == 31) {
+            s_misc[4 + warp] = ic;
+            s_misc[12 + warp] = ib;
+        }
+        tile_excl = ic - cnt;
+        bin_excl = ib - bin;
+    }
+    if (a.look_clear != nullptr)
+        for (uint32_t i = tid; i < 256; i += T) a.look_clear[tile * 256 + i] = 0;
+    __syncthreads();
+    if (tid < 256) {
+        for (uint32_t w = 0; w < warp; ++w) {
+            tile_excl += s_misc[4 + w];
+            bin_excl += s_misc[12 + w];
+        }
+        // s_cnt[w][d]: tile slot where warp w's first key of digit d goes
+#pragma unroll
+        for (int w = 0; w < WARPS; ++w) s_cnt[w * kRow + tid] += tile_excl;
+    }
+    __syncthreads();
+
+    // ---- decoupled look-back, one digit per thread of the first 8 warps
+    // (the other warps rank meanwhile); then publish this tile's prefixes
+    if (tid < 256) {
+        uint32_t excl = 0;
+        bool ok = true;
+        if (tile > 0 && tile != a.stall_tile) {
+            ok = look_back<LW>(a, tile, tid, excl);
+            if (ok) st_relaxed(a.look + tile * 256 + tid, kFlagPrefix | (excl + cnt));
+        }
+        if (!ok) {
+            s_misc[2] = 1;
+            record_error(a.status, a.abort_flag, GSORT_ETIMEOUT);
+        }
+        // global index of tile slot i holding digit d: s_goff[d] + i
+        s_goff[tid] = bin_excl + excl - tile_excl;
+    }
+
+    // ---- warp multisplit: stable slot of each key in the tile-sorted order
+    {
+        uint32_t *wc = s_cnt + warp * kRow;
+        const uint32_t ltm = lanemask_lt();
+        const LaneConsts c = lane_consts(lane);
+#pragma unroll
+        for (int k = 0; k < IPT; ++k) {
+            const bool valid = FULL || item0 + k * 32 < tile_n;
+            const uint32_t d = valid ? digit_at<BYTE>(key[k], a.shift, a.mask) : 0u;
+            uint32_t peers = digit_peers<MATCH>(d, c);
+            if (!FULL) peers &= __ballot_sync(kFullMask, valid);
+            const uint32_t leader = highest_bit(peers);   // peers is empty only for padding lanes
+            uint32_t base = 0;
+            if (valid && lane == leader)
+                base = atomicAdd(&wc[d], static_cast<uint32_t>(__popc(peers)));
+            base = __shfl_sync(kFullMask, base, leader);
+            if (valid) {
+                const uint32_t slot = base + __popc(peers & ltm);
+                s_keys[slot] = key[k];
+                if (PAIRS) s_vals[slot] = val[k];
+            }
+        }
+    }
+    __syncthreads();
+    before_output();
+    if (s_misc[2] || tile == a.stall_tile) return false;
+
+    // ---- contiguous runs per digit out to global memory
+    K *dst_k = static_cast<K *>(a.dst_k);
+#pragma unroll
+    for (int k = 0; k < IPT; ++k) {
+        const uint32_t i = k * T + tid;
+        if (FULL || i < tile_n) {
+            const K kk = s_keys[i];
+            const uint32_t g = s_goff[digit_at<BYTE>(kk, a.shift, a.mask)] + i;
+            if (g < a.n) {
+                dst_k[g] = XOUT ? order_out<K>(kk, static_cast<K>(a.fmask), static_cast<K>(a.flip)) : kk;
+                if (PAIRS) a.dst_v[g] = s_vals[i];
+            }
+        }
+    }
+    return true;
+}
+
+template <class K, int WARPS, int IPT, int MINB, int MATCH, int LW, bool BYTE, bool PAIRS, bool XIN,
+          bool XOUT>
+__global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass(const PassArgs a) {
+    constexpr int TILE = WARPS * 32 * IPT;
+    extern __shared__ __align__(128) uint32_t smem[];
+    uint32_t *s_misc = smem + pass_smem_words<K, WARPS, IPT, PAIRS>() - 32;
+    const uint32_t tid = threadIdx.x;
+    if (tid == 0) {
+        s_misc[0] = atomicAdd(a.tile_counter, 1u);   // tiles in start order: look-back always progresses
+        s_misc[1] = ld_relaxed(a.abort_flag);
+        s_misc[2] = 0;
+    }
+    constexpr size_t kKeyWords = sizeof(K) / 4;
+    uint32_t *s_cnt = smem + TILE * (kKeyWords + (PAIRS ? 1 : 0));
+    for (uint32_t i = tid; i < WARPS * kRow; i += WARPS * 32) s_cnt[i] = 0;
+    __syncthreads();
+    const uint32_t tile = s_misc[0];
+    if (s_misc[1]) return;   // an earlier wait gave up; the result is void anyway
+    K *s_keys = reinterpret_cast<K *>(smem);
+    uint32_t *s_vals = smem + TILE * kKeyWords;
+    const K *kin = static_cast<const K *>(a.src_k) + tile * TILE;
+    const uint32_t *vin = PAIRS ? a.src_v + tile * TILE : nullptr;
+    if (a.n - tile * TILE >= static_cast<uint32_t>(TILE))
+        pass_tile<K, WARPS, IPT, MATCH, LW, BYTE, PAIRS, XIN, XOUT, true>(a, s_cnt, tile, kin, vin, s_keys, s_vals);
+    else
+        pass_tile<K, WARPS, IPT, MATCH, LW, BYTE, PAIRS, XIN, XOUT, false>(a, s_cnt, tile, kin, vin, s_keys, s_vals);
+}
+
+// One-tile-per-CTA launch configuration of the digit pass.
+template <class K, int WARPS, int IPT, int MINB, int MATCH, int LW = 8>
+struct PassConfig {
+    static constexpr uint32_t kTile = WARPS * 32 * IPT;
+
+    template <bool B, bool P, bool XI, bool XO>
+    static cudaError_t launch_one(const PassArgs &a, uint32_t tiles, cudaStream_t s) {
+        auto k = k_digit_pass<K, WARPS, IPT, MINB, MATCH, LW, B, P, XI, XO>;
+        const size_t smem = pass_smem_words<K, WARPS, IPT, P>() * sizeof(uint32_t);
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        k<<<tiles, WARPS * 32, smem, s>>>(a);
+        return cudaGetLastError();
+    }
+
+    template <bool B>
+    static cudaError_t launch_b(const PassArgs &a, bool pairs, bool xin, bool xout, uint32_t tiles,
+                                cudaStream_t s) {
+        const int sel = (pairs ? 4 : 0) | (xin ? 2 : 0) | (xout ? 1 : 0);
+        switch (sel) {
+            case 0: return launch_one<B, false, false, false>(a, tiles, s);
+            case 1: return launch_one<B, false, false, true>(a, tiles, s);
+            case 2: return launch_one<B, false, true, false>(a, tiles, s);
+            case 3: return launch_one<B, false, true, true>(a, tiles, s);
+            case 4: return launch_one<B, true, false, false>(a, tiles, s);
+            case 5: return launch_one<B, true, false, true>(a, tiles, s);
+            case 6: return launch_one<B, true, true, false>(a, tiles, s);
+            default: return launch_one<B, true, true, true>(a, tiles, s);
+        }
+    }
+
+    static cudaError_t launch(const PassArgs &a, bool pairs, bool xin, bool xout, uint32_t tiles,
+                              cudaStream_t s) {
+        const bool byte = (a.shift % 8) == 0 && a.mask == 0xFFu;
+        return byte ? launch_b<true>(a, pairs, xin, xout, tiles, s)
+                    : launch_b<false>(a, pairs, xin, xout, tiles, s);
+    }
+};
+
+// Histogram launch: one CTA per SM (fewer for small inputs: about 16 keys per
+// thread at least).
+template <class K>
+cudaError_t launch_hist_kernel(const K *keys, uint32_t n, bool xf, K fmask, K flip, int begin_bit,
+                               int passes, uint32_t last_mask, uint32_t *hist, uint32_t *clear,
+                               uint32_t clear_words, cudaStream_t s, int sm_count) {
+    const uint32_t want = (n + kHistThreads * 16 - 1) / (kHistThreads * 16);
+    const uint32_t grid = std::max(1u, std::min(want, static_cast<uint32_t>(sm_count)));
+    uint4 *cl = reinterpret_cast<uint4 *>(clear);
+    const bool byte = (begin_bit % 8) == 0 && last_mask == 0xFFu;
+    auto k = xf ? (byte ? k_digit_hist<K, true, true> : k_digit_hist<K, true, false>)
+                : (byte ? k_digit_hist<K, false, true> : k_digit_hist<K, false, false>);
+    const size_t smem = static_cast<size_t>(passes) * (sizeof(K) == 8 ? 128 : 256) * 32 * sizeof(uint32_t);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kHistSmemBytes));
+    if (e != cudaSuccess) return e;
+    k<<<grid, kHistThreads, smem, s>>>(keys, n, begin_bit, passes, last_mask, fmask, flip, hist, cl,
+                                       clear_words / 4);
+    return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace gsort

@@ -6,9 +6,12 @@ CUDA stream, and raise GsortError on a non-zero status.  There is no CPU
 fallback: CPU tensors are copied to the current CUDA device, processed there
 and copied back.
 
-Keys are 32-bit: torch.uint32 or torch.int32 tensors are sorted as unsigned
-32-bit integers (an int32 tensor is a container of bit patterns here), and
-torch.float32 tensors are sorted in IEEE totalOrder (-0.0 before +0.0).
+sort_pairs/sort_keys take 32-bit keys: torch.uint32 or torch.int32 tensors are
+sorted as unsigned 32-bit integers (an int32 tensor is a container of bit
+patterns there), and torch.float32 tensors in IEEE totalOrder (-0.0 before
++0.0).  sort() takes every key kind, with the kind read from the dtype
+(int32/int64 signed, uint32/uint64 unsigned, float32/float64 totalOrder)
+unless given, in either direction.
 """
 from __future__ import annotations
 
@@ -19,8 +22,16 @@ import torch
 from . import _lib
 from .build import build  # noqa: F401  (re-exported)
 
-KEY_U32, KEY_F32 = 0, 1
+KEY_U32, KEY_F32, KEY_I32, KEY_U64, KEY_F64, KEY_I64 = 0, 1, 2, 3, 4, 5
+DESCENDING = 1
 _U32_DTYPES = (torch.int32,) + ((torch.uint32,) if hasattr(torch, "uint32") else ())
+_KIND_OF_DTYPE = {torch.float32: KEY_F32, torch.int32: KEY_I32, torch.float64: KEY_F64,
+                  torch.int64: KEY_I64}
+if hasattr(torch, "uint32"):
+    _KIND_OF_DTYPE[torch.uint32] = KEY_U32
+if hasattr(torch, "uint64"):
+    _KIND_OF_DTYPE[torch.uint64] = KEY_U64
+_KIND_BYTES = {KEY_U32: 4, KEY_F32: 4, KEY_I32: 4, KEY_U64: 8, KEY_F64: 8, KEY_I64: 8}
 
 
 class GsortError(RuntimeError):
@@ -129,6 +140,60 @@ def sort_pairs(keys: torch.Tensor, values: torch.Tensor | None = None, begin_bit
     return ko, vo
 
 
+def sort_workspace_bytes(n: int, kind: int, with_values: bool) -> int:
+    return int(_lib.load().gsort_radix_sort_workspace_bytes(n, kind, 1 if with_values else 0))
+
+
+def sort(keys: torch.Tensor, values: torch.Tensor | None = None, *, descending: bool = False,
+         kind: int | None = None, begin_bit: int = 0, end_bit: int | None = None,
+         keys_out: torch.Tensor | None = None, values_out: torch.Tensor | None = None,
+         workspace: torch.Tensor | None = None, events=None, spin_limit: int = 0,
+         stall_tile: int = -1, check: bool = True):
+    """Stable radix sort of 32- or 64-bit keys (and 32-bit values), ascending
+    or descending, by bits [begin_bit, end_bit) of the mapped key (default:
+    the whole key).  Returns (sorted_keys, sorted_values or None)."""
+    if not keys.is_cuda:
+        return _host_roundtrip(
+            lambda k, v: sort(k, v, descending=descending, kind=kind, begin_bit=begin_bit,
+                              end_bit=end_bit), keys, values)
+    k = _flat_cuda(keys, "keys")
+    if kind is None:
+        if k.dtype not in _KIND_OF_DTYPE:
+            raise TypeError(f"no key kind for dtype {k.dtype}; pass kind=")
+        kind = _KIND_OF_DTYPE[k.dtype]
+    if _KIND_BYTES.get(kind) != k.element_size():
+        raise TypeError(f"kind {kind} needs {_KIND_BYTES.get(kind)}-byte keys, got {k.dtype}")
+    if end_bit is None:
+        end_bit = 8 * k.element_size()
+    v = None
+    if values is not None:
+        v = _flat_cuda(values, "values")
+        if v.numel() != k.numel() or v.element_size() != 4:
+            raise ValueError("values must be a 32-bit tensor with one entry per key")
+    n = k.numel()
+    ko = torch.empty_like(k) if keys_out is None else _flat_cuda(keys_out, "keys_out")
+    vo = None
+    if v is not None:
+        vo = torch.empty_like(v) if values_out is None else _flat_cuda(values_out, "values_out")
+    lib = _lib.load()
+    ws = _workspace(sort_workspace_bytes(n, kind, v is not None), k.device, workspace)
+    ev, nev = _events_arg(events)
+    opt = _lib.Options(spin_limit, stall_tile, ctypes.cast(ev, ctypes.POINTER(ctypes.c_void_p))
+                       if ev is not None else None, nev, 0)
+    with torch.cuda.device(k.device):
+        rc = lib.gsort_radix_sort_ex(
+            k.data_ptr(), ko.data_ptr(), v.data_ptr() if v is not None else None,
+            vo.data_ptr() if vo is not None else None, n, kind, DESCENDING if descending else 0,
+            begin_bit, end_bit, ws.data_ptr(), ws.numel(), _stream(k.device), ctypes.byref(opt))
+        _check(rc, "gsort_radix_sort")
+        if check and n > 0 and begin_bit < end_bit:
+            _check(lib.gsort_check(ws.data_ptr(), _stream(k.device)), "gsort_radix_sort (device)")
+    ko = ko.view(keys.shape) if keys_out is None else keys_out
+    if vo is not None:
+        vo = vo.view(values.shape) if values_out is None else values_out
+    return ko, vo
+
+
 def sort_keys(keys: torch.Tensor, **kw) -> torch.Tensor:
     """Ascending sort of 32-bit keys (all 32 bits)."""
     if not keys.is_cuda:
@@ -137,10 +202,19 @@ def sort_keys(keys: torch.Tensor, **kw) -> torch.Tensor:
     return sort_pairs(keys, None, 0, 32, keys_out=ko, **kw)[0]
 
 
-def digit_histograms(keys: torch.Tensor, begin_bit: int = 0, end_bit: int = 32) -> torch.Tensor:
-    """[passes, 256] counts of each 8-bit digit (int32 tensor holding uint32 counts)."""
+def digit_histograms(keys: torch.Tensor, begin_bit: int = 0, end_bit: int | None = None, *,
+                     kind: int | None = None) -> torch.Tensor:
+    """[passes, 256] counts of each 8-bit digit of the (ascending) mapped key
+    (int32 tensor holding uint32 counts).  Without `kind`, 32-bit tensors are
+    read as sort_keys reads them (int32/uint32 unsigned, float32 totalOrder)
+    and 64-bit tensors by their dtype."""
     k = _flat_cuda(keys, "keys")
-    kind = _key_kind(k)
+    if kind is None:
+        kind = _key_kind(k) if k.element_size() == 4 else _KIND_OF_DTYPE.get(k.dtype)
+        if kind is None:
+            raise TypeError(f"no key kind for dtype {k.dtype}; pass kind=")
+    if end_bit is None:
+        end_bit = 8 * k.element_size()
     passes = (end_bit - begin_bit + 7) // 8
     out = torch.empty((max(passes, 1), 256), dtype=torch.int32, device=k.device)
     with torch.cuda.device(k.device):

@@ -5,7 +5,9 @@
 
 OP: keys (uint32 keys, 32 bits), pairs (uint32 key/index pairs), fpairs
 (float keys with index values), compact (compaction input), segments (1024-key
-segments, n/1024 of them), hist (the digit-histogram step alone).
+segments, n/1024 of them), hist (the digit-histogram step alone), sort (any
+key kind: --kind u32|f32|i32|u64|f64|i64 [--desc] [--values]).
+--time prints the median CUDA-event time of the timed calls.
 Each call is followed by a device-status check; the process exits non-zero on
 any error, so a profiler only ever runs a command that finished cleanly.
 """
@@ -22,7 +24,11 @@ from . import _lib, gsort, synth
 
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=["keys", "pairs", "fpairs", "compact", "segments", "hist"])
+    ap.add_argument("op", choices=["keys", "pairs", "fpairs", "compact", "segments", "hist", "sort"])
+    ap.add_argument("--kind", choices=["u32", "f32", "i32", "u64", "f64", "i64"], default="u64")
+    ap.add_argument("--desc", action="store_true")
+    ap.add_argument("--values", action="store_true")
+    ap.add_argument("--time", action="store_true")
     ap.add_argument("--n-log2", type=int, default=26)
     ap.add_argument("--warmup", type=int, default=1)
     ap.add_argument("--reps", type=int, default=1)
@@ -35,7 +41,14 @@ def main(argv=None) -> int:
         x = np.ascontiguousarray(x)
         return torch.from_numpy(x.view(np.int32) if x.dtype == np.uint32 else x).to(dev)
 
-    if a.op in ("keys", "hist"):
+    kinds = {"u32": 0, "f32": 1, "i32": 2, "u64": 3, "f64": 4, "i64": 5}
+    kind = kinds[a.kind]
+    if a.op == "sort":
+        kx = synth.keys_of_kind(kind, n, 6)
+        kx = kx.view({4: np.int32, 8: np.int64}[kx.dtype.itemsize]) if kx.dtype.kind == "u" else kx
+        x = torch.from_numpy(np.ascontiguousarray(kx)).to(dev)
+        v = up(synth.index_values(n)) if a.values else None
+    elif a.op in ("keys", "hist"):
         x = up(synth.uniform_keys(n, 1))
     elif a.op == "pairs":
         x, v = up(synth.uniform_keys(n, 2)), up(synth.index_values(n))
@@ -48,7 +61,9 @@ def main(argv=None) -> int:
         x = seg.clone()
 
     def once():
-        if a.op == "keys":
+        if a.op == "sort":
+            gsort.sort(x, v, descending=a.desc, kind=kind, check=not a.time)
+        elif a.op == "keys":
             gsort.sort_pairs(x, None, variant=a.variant)
         elif a.op in ("pairs", "fpairs"):
             gsort.sort_pairs(x, v, variant=a.variant)
@@ -60,9 +75,20 @@ def main(argv=None) -> int:
             x.copy_(seg)
             gsort.segmented_sort_(x.view(-1, 1024))
 
-    for _ in range(a.warmup + a.reps):
+    for _ in range(a.warmup):
         once()
-    torch.cuda.synchronize()
+    times = []
+    for _ in range(a.reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        once()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    if a.time:
+        ms = float(np.median(times))
+        print(f"{a.op} {a.kind if a.op == 'sort' else ''} desc={a.desc} values={a.values}: "
+              f"median {ms:.4f} ms per call over {a.reps}, {n / ms / 1e6:.2f} Gkeys/s")
     print(f"{a.op}: n=2^{a.n_log2} warmup={a.warmup} reps={a.reps} variant={a.variant} "
           f"({_lib.load().gsort_radix_variant_name(a.variant).decode()}) ok")
     return 0

@@ -132,6 +132,43 @@ def normal_f32_with_specials(n: int, seed: int = SEED_BASE) -> np.ndarray:
     return x
 
 
+def normal_with_specials(n: int, dtype=np.float64, seed: int = SEED_BASE) -> np.ndarray:
+    """normal_f32_with_specials at another float width (float64: no rounding)."""
+    u1 = u01(stream_seed(seed, 0), n)
+    u2 = u01(stream_seed(seed, 1), n)
+    x = (np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)).astype(dtype)
+    q = n // 100
+    if q > 0:
+        r = splitmix64(stream_seed(seed, 2), n)
+        chosen = np.argpartition(r, 4 * q - 1)[: 4 * q]
+        chosen = chosen[np.argsort(r[chosen], kind="stable")]
+        for j, v in enumerate((0.0, -0.0, np.inf, -np.inf)):
+            x[chosen[j * q:(j + 1) * q]] = dtype(v)
+    return x
+
+
+def keys64(n: int, seed: int = SEED_BASE) -> np.ndarray:
+    """uint64 keys uniform over [0, 2^64): one splitmix64 word per key."""
+    return splitmix64(stream_seed(seed, 3), n)
+
+
+def keys_of_kind(kind: int, n: int, seed: int = SEED_BASE) -> np.ndarray:
+    """Seeded keys of a key kind (0 u32, 1 f32, 2 i32, 3 u64, 4 f64, 5 i64),
+    uniform over the bit patterns for integers, normal with +-0 and +-inf
+    for floats, with a share of repeated keys so that stability matters."""
+    if kind in (0, 2):
+        k = uniform_keys(n, seed).view(np.int32 if kind == 2 else np.uint32)
+    elif kind in (3, 5):
+        k = keys64(n, seed).view(np.int64 if kind == 5 else np.uint64)
+    else:
+        k = normal_with_specials(n, np.float32 if kind == 1 else np.float64, seed)
+    if n >= 8:
+        r = splitmix64(stream_seed(seed, 4), n // 8) % np.uint64(n)
+        k = k.copy()
+        k[r.astype(np.int64)] = k[: n // 8]   # about an eighth of the keys repeat earlier ones
+    return k
+
+
 def compaction_input(n: int, seed: int = SEED_BASE) -> np.ndarray:
     """float32 drawn from {-U(0,1), 0.0, +U(0,1)} with probabilities
     0.4 / 0.2 / 0.4 (category from one stream, magnitude from another)."""

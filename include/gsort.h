@@ -58,8 +58,15 @@ typedef enum gsort_status {
 
 typedef enum gsort_key_kind {
     GSORT_KEY_U32 = 0,      /* unsigned 32-bit integers */
-    GSORT_KEY_F32 = 1       /* IEEE-754 binary32, ordered as totalOrder for non-NaN */
+    GSORT_KEY_F32 = 1,      /* IEEE-754 binary32, ordered as totalOrder for non-NaN */
+    GSORT_KEY_I32 = 2,      /* two's-complement 32-bit integers */
+    GSORT_KEY_U64 = 3,      /* unsigned 64-bit integers */
+    GSORT_KEY_F64 = 4,      /* IEEE-754 binary64, ordered as totalOrder for non-NaN */
+    GSORT_KEY_I64 = 5       /* two's-complement 64-bit integers */
 } gsort_key_kind;
+
+/* Flags of gsort_radix_sort(). */
+#define GSORT_DESCENDING 1  /* largest key first; equal keys keep their input order */
 
 #define GSORT_MAX_N ((int64_t)((1 << 30) - 1))
 
@@ -94,16 +101,18 @@ int gsort_version(void);
  * state regions and one ping-pong buffer per sorted array. */
 size_t gsort_radix_workspace_bytes(int64_t n, int with_values);
 
-/* Sort n keys ascending by all 32 bits.  d_keys_in is not modified unless
- * it equals d_keys_out (in place is allowed).  Partially overlapping
- * buffers: GSORT_EINVAL. */
+/* Sort n 32-bit keys (kind GSORT_KEY_U32, F32 or I32) ascending by all 32
+ * bits.  d_keys_in is not modified unless it equals d_keys_out (in place is
+ * allowed).  Partially overlapping buffers: GSORT_EINVAL. */
 int gsort_radix_keys(const void *d_keys_in, void *d_keys_out, int64_t n,
                      int kind, void *d_ws, size_t ws_bytes, cudaStream_t stream);
 
 /* Stable sort of (key, value) pairs by key bits [begin_bit, end_bit)
- * (0 <= begin_bit <= end_bit <= 32).  Bits outside the range do not take
- * part in the order but are carried.  begin_bit == end_bit copies.  For
- * kind == GSORT_KEY_F32 the range applies to the mapped key (use 0..32).
+ * (0 <= begin_bit <= end_bit <= 32) for the 32-bit kinds U32, F32 and I32
+ * (other kinds: GSORT_EINVAL; gsort_radix_sort takes every kind).  Bits
+ * outside the range do not take part in the order but are carried.
+ * begin_bit == end_bit copies.  For F32 and I32 the range applies to the
+ * mapped key (use 0..32).
  * d_vals_in and d_vals_out are both NULL (keys only) or both non-NULL.
  * In-place (in == out) is allowed for keys and for values. */
 int gsort_radix_pairs(const void *d_keys_in, void *d_keys_out,
@@ -111,10 +120,40 @@ int gsort_radix_pairs(const void *d_keys_in, void *d_keys_out,
                       int kind, int begin_bit, int end_bit,
                       void *d_ws, size_t ws_bytes, cudaStream_t stream);
 
+/* ------------------------------------------------------------------------
+ * General radix sort: every key kind, ascending or descending.
+ * ([PMPP10] section 8, exercises 2 (64-bit keys: 8 passes of radix 256),
+ * 6 (descending order) and 7 (float keys); signed keys flip the sign bit,
+ * the same idea for two's complement.)
+ *
+ * Stable sort of n keys of `kind` (4- or 8-byte words, see gsort_key_kind),
+ * with optional 32-bit values, by the bits [begin_bit, end_bit) of the
+ * mapped key: the key's bit pattern taken through the order map of its kind
+ * (identity for unsigned, sign bit flipped for signed, the totalOrder map for
+ * floats), complemented when flags has GSORT_DESCENDING.  0 <= begin_bit <=
+ * end_bit <= 8 * key bytes; 0..32 or 0..64 sorts by the whole key.  Equal
+ * (masked) keys keep their input order in both directions.  Output keys
+ * hold the original bit patterns.
+ *
+ * Keys must be aligned to their size (else GSORT_EALIGN), values to 4 bytes.
+ * In place, aliasing and NULL rules as for gsort_radix_pairs.  flags other
+ * than 0 and GSORT_DESCENDING: GSORT_EINVAL.  The workspace comes from
+ * gsort_radix_sort_workspace_bytes() with the same kind; for 32-bit kinds it
+ * equals gsort_radix_workspace_bytes().
+ * ---------------------------------------------------------------------- */
+size_t gsort_radix_sort_workspace_bytes(int64_t n, int kind, int with_values);
+
+int gsort_radix_sort(const void *d_keys_in, void *d_keys_out,
+                     const uint32_t *d_vals_in, uint32_t *d_vals_out, int64_t n,
+                     int kind, int flags, int begin_bit, int end_bit,
+                     void *d_ws, size_t ws_bytes, cudaStream_t stream);
+
 /* The upfront histogram step on its own: d_hist_out receives
  * passes * 256 uint32 counts, passes = ceil((end_bit - begin_bit) / 8);
  * entry [p * 256 + d] counts the keys whose p-th 8-bit digit (from
- * begin_bit, last digit narrowed to end_bit) is d.  Needs no workspace. */
+ * begin_bit, last digit narrowed to end_bit) of the mapped key (ascending
+ * order map of `kind`, any kind; end_bit <= 8 * key bytes) is d.  Needs no
+ * workspace. */
 int gsort_digit_histograms(const void *d_keys, int64_t n, int kind,
                            int begin_bit, int end_bit, uint32_t *d_hist_out,
                            cudaStream_t stream);
@@ -197,8 +236,9 @@ typedef struct gsort_options {
      * entries are left alone; missing ones are skipped. */
     void **events;
     int num_events;
-    /* Launch configuration of the digit passes (0 = default; see
-     * gsort_radix_variant_name()). */
+    /* Launch configuration of the digit passes of 32-bit keys (0 = default;
+     * see gsort_radix_variant_name()); 64-bit keys have one configuration
+     * and accept only 0. */
     int variant;
 } gsort_options;
 
@@ -207,6 +247,12 @@ int gsort_radix_pairs_ex(const void *d_keys_in, void *d_keys_out,
                          int kind, int begin_bit, int end_bit,
                          void *d_ws, size_t ws_bytes, cudaStream_t stream,
                          const gsort_options *options);
+
+int gsort_radix_sort_ex(const void *d_keys_in, void *d_keys_out,
+                        const uint32_t *d_vals_in, uint32_t *d_vals_out, int64_t n,
+                        int kind, int flags, int begin_bit, int end_bit,
+                        void *d_ws, size_t ws_bytes, cudaStream_t stream,
+                        const gsort_options *options);
 
 int gsort_compact_positive_ex(const float *d_in, float *d_out, int64_t n,
                               int64_t *d_num_kept, void *d_ws, size_t ws_bytes,
@@ -219,8 +265,11 @@ const char *gsort_radix_variant_name(int variant);
 
 /* Kernel launches one call makes (for launch accounting):
  * radix: 2 + passes (+1 copy-back when sorting in place with an odd pass
- * count); compaction: 3; segmented: 1 (0 when there is nothing to do). */
+ * count; +1 histogram clear for 64-bit keys, see
+ * gsort_radix_sort_launch_count); compaction: 3; segmented: 1 (0 when
+ * there is nothing to do). */
 int gsort_radix_launch_count(int64_t n, int begin_bit, int end_bit, int in_place);
+int gsort_radix_sort_launch_count(int64_t n, int kind, int begin_bit, int end_bit, int in_place);
 
 #ifdef __cplusplus
 }

@@ -204,6 +204,169 @@ int oracle_radix_sort_keys(const uint32_t *keys_in, uint32_t *keys_out,
 }
 
 /* ---------------------------------------------------------------------------
+ * NEXT (f1): every key kind, ascending or descending.
+ *   kinds: 0 u32, 1 f32, 2 i32, 3 u64, 4 f64, 5 i64 (4- or 8-byte words).
+ * The key is replaced by an unsigned "ordered" value of its own width whose
+ * unsigned order is the wanted order, sorted by the same stable LSD counting
+ * passes as above ([CUDA3] "Radix Sort", CPU version), and mapped back.
+ *   - signed: value + 2^(w-1), i.e. the signed range shifted onto the
+ *     unsigned one (the pages do not cover signed keys; this is the plain
+ *     reading of "sort the signed values");
+ *   - float: the IEEE totalOrder map of a0, at 32 or 64 bits ([PMPP10]
+ *     exercise 7);
+ *   - descending: (2^w - 1) - ordered, which reverses the order of distinct
+ *     values and leaves equal values equal, so the stable passes keep equal
+ *     keys in input order ([PMPP10] exercise 6);
+ *   - 64-bit keys take (end_bit - begin_bit)/8 = 8 passes for the whole key
+ *     ([PMPP10] exercise 2: radix 256 on 64-bit integers).
+ * ------------------------------------------------------------------------- */
+int oracle_kind_bytes(int kind)
+{
+    switch (kind) {
+    case 0: case 1: case 2: return 4;
+    case 3: case 4: case 5: return 8;
+    default: return 0;
+    }
+}
+
+uint64_t oracle_key_to_ordered(uint64_t bits, int kind, int descending)
+{
+    uint64_t u;
+    int w = oracle_kind_bytes(kind) * 8;
+    switch (kind) {
+    case 0: u = bits & 0xFFFFFFFFull; break;
+    case 1: u = oracle_f32_bits_to_ordered((uint32_t)bits); break;
+    case 2: u = (uint64_t)((int64_t)(int32_t)(uint32_t)bits + 2147483648LL); break;
+    case 3: u = bits; break;
+    case 4:
+        if (bits >> 63)
+            u = ~bits;
+        else
+            u = bits | 0x8000000000000000ull;
+        break;
+    case 5: u = bits + 0x8000000000000000ull; break;   /* value + 2^63, modulo 2^64 */
+    default: return 0;
+    }
+    if (descending)
+        u = (w == 64 ? 0xFFFFFFFFFFFFFFFFull : 0xFFFFFFFFull) - u;
+    return u;
+}
+
+uint64_t oracle_ordered_to_key(uint64_t u, int kind, int descending)
+{
+    int w = oracle_kind_bytes(kind) * 8;
+    if (descending)
+        u = (w == 64 ? 0xFFFFFFFFFFFFFFFFull : 0xFFFFFFFFull) - u;
+    switch (kind) {
+    case 0: return u & 0xFFFFFFFFull;
+    case 1: return oracle_ordered_to_f32_bits((uint32_t)u);
+    case 2: return (uint64_t)(uint32_t)(int32_t)((int64_t)u - 2147483648LL);
+    case 3: return u;
+    case 4:
+        if (u >> 63)
+            return u & 0x7FFFFFFFFFFFFFFFull;
+        return ~u;
+    case 5: return u - 0x8000000000000000ull;
+    default: return 0;
+    }
+}
+
+static uint64_t load_key(const void *keys, int64_t i, int kb)
+{
+    if (kb == 4)
+        return ((const uint32_t *)keys)[i];
+    return ((const uint64_t *)keys)[i];
+}
+
+static void store_key(void *keys, int64_t i, int kb, uint64_t v)
+{
+    if (kb == 4)
+        ((uint32_t *)keys)[i] = (uint32_t)v;
+    else
+        ((uint64_t *)keys)[i] = v;
+}
+
+/* The p-th digit of a 64-bit ordered value: bits [begin_bit + 8p, min(+8, end_bit)). */
+static uint32_t digit_of64(uint64_t k, int begin_bit, int end_bit, int p)
+{
+    int lo = begin_bit + 8 * p;
+    int width = end_bit - lo;
+    if (width > 8)
+        width = 8;
+    return (uint32_t)((k >> lo) & ((1ull << width) - 1ull));
+}
+
+int oracle_digit_histograms_general(const void *keys, int64_t n, int kind, int flags,
+                                    int begin_bit, int end_bit, uint32_t *hist)
+{
+    int kb = oracle_kind_bytes(kind);
+    if (kb == 0 || n < 0 || begin_bit < 0 || end_bit > 8 * kb || begin_bit > end_bit)
+        return ORACLE_EINVAL;
+    int passes = (end_bit - begin_bit + 7) / 8;
+    memset(hist, 0, sizeof(uint32_t) * 256 * (size_t)(passes > 0 ? passes : 1));
+    for (int64_t i = 0; i < n; ++i) {
+        uint64_t k = oracle_key_to_ordered(load_key(keys, i, kb), kind, flags & 1);
+        for (int p = 0; p < passes; ++p)
+            hist[p * 256 + digit_of64(k, begin_bit, end_bit, p)] += 1;
+    }
+    return ORACLE_OK;
+}
+
+int oracle_radix_sort_general(const void *keys_in, const uint32_t *vals_in,
+                              void *keys_out, uint32_t *vals_out, int64_t n,
+                              int kind, int flags, int begin_bit, int end_bit)
+{
+    int kb = oracle_kind_bytes(kind);
+    if (kb == 0 || n < 0 || (flags & ~1) != 0 || begin_bit < 0 || end_bit > 8 * kb ||
+        begin_bit > end_bit)
+        return ORACLE_EINVAL;
+    if (n == 0)
+        return ORACLE_OK;
+    int passes = (end_bit - begin_bit + 7) / 8;
+    int with_vals = (vals_in != NULL && vals_out != NULL);
+    uint64_t *x = malloc(sizeof(uint64_t) * (size_t)n);
+    uint64_t *y = malloc(sizeof(uint64_t) * (size_t)n);
+    uint32_t *vx = with_vals ? malloc(sizeof(uint32_t) * (size_t)n) : NULL;
+    uint32_t *vy = with_vals ? malloc(sizeof(uint32_t) * (size_t)n) : NULL;
+    if (!x || !y || (with_vals && (!vx || !vy))) {
+        free(x); free(y); free(vx); free(vy);
+        return ORACLE_ENOMEM;
+    }
+    for (int64_t i = 0; i < n; ++i) {
+        x[i] = oracle_key_to_ordered(load_key(keys_in, i, kb), kind, flags & 1);
+        if (with_vals)
+            vx[i] = vals_in[i];
+    }
+    for (int p = 0; p < passes; ++p) {
+        uint32_t count[256];
+        uint32_t next[256];
+        memset(count, 0, sizeof(count));
+        for (int64_t i = 0; i < n; ++i)
+            count[digit_of64(x[i], begin_bit, end_bit, p)] += 1;
+        uint32_t running = 0;
+        for (int d = 0; d < 256; ++d) {
+            next[d] = running;
+            running += count[d];
+        }
+        for (int64_t i = 0; i < n; ++i) {
+            uint32_t slot = next[digit_of64(x[i], begin_bit, end_bit, p)]++;
+            y[slot] = x[i];
+            if (with_vals)
+                vy[slot] = vx[i];
+        }
+        uint64_t *t = x; x = y; y = t;
+        if (with_vals) { uint32_t *tv = vx; vx = vy; vy = tv; }
+    }
+    for (int64_t i = 0; i < n; ++i) {
+        store_key(keys_out, i, kb, oracle_ordered_to_key(x[i], kind, flags & 1));
+        if (with_vals)
+            vals_out[i] = vx[i];
+    }
+    free(x); free(y); free(vx); free(vy);
+    return ORACLE_OK;
+}
+
+/* ---------------------------------------------------------------------------
  * a4: stream compaction, the 1-bit special case ([CUDA3] "Stream
  * Compaction": predicate, exclusive scan of the predicate, scatter).  Keeps
  * every x > 0 in input order at out[0..m), writes +0.0 to out[m..n), and

@@ -58,6 +58,21 @@ def _as_u32(a) -> np.ndarray:
     return a
 
 
+# numpy dtype of each key kind (u32, f32, i32, u64, f64, i64)
+KIND_DTYPES = (np.uint32, np.float32, np.int32, np.uint64, np.float64, np.int64)
+
+
+def _as_kind(a, kind: int) -> np.ndarray:
+    """Contiguous 1-D array of the key kind's dtype (same bits, no conversion)."""
+    a = np.ascontiguousarray(a).ravel()
+    want = np.dtype(KIND_DTYPES[kind])
+    if a.dtype != want:
+        if a.dtype.itemsize != want.itemsize:
+            raise TypeError(f"kind {kind} wants {want.itemsize}-byte keys, got {a.dtype}")
+        a = a.view(want)
+    return a
+
+
 def _ptr(a):
     return None if a is None else a.ctypes.data_as(_u32p)
 
@@ -84,6 +99,13 @@ class Oracle:
         "oracle_segmented_sort": (_int, [_u32p, _i64, _int]),
         "oracle_bitonic_network": (_int, [_u32p, _int]),
         "oracle_radix2_three_pass": (_int, [_u32p, _u32p, _u32p, _u32p, _i64]),
+        "oracle_kind_bytes": (_int, [_int]),
+        "oracle_key_to_ordered": (ctypes.c_uint64, [ctypes.c_uint64, _int, _int]),
+        "oracle_ordered_to_key": (ctypes.c_uint64, [ctypes.c_uint64, _int, _int]),
+        "oracle_digit_histograms_general": (_int, [ctypes.c_void_p, _i64, _int, _int, _int, _int,
+                                                   _u32p]),
+        "oracle_radix_sort_general": (_int, [ctypes.c_void_p, _u32p, ctypes.c_void_p, _u32p, _i64,
+                                             _int, _int, _int, _int]),
     }
 
     def __init__(self, path: str):
@@ -156,6 +178,43 @@ class Oracle:
 
     def radix_sort_keys(self, keys, kind: int = 0) -> np.ndarray:
         return self.radix_sort_pairs(keys, None, kind, 0, 32)[0]
+
+    # f1: every key kind, both directions ------------------------------
+    def key_to_ordered(self, bits: int, kind: int, descending: bool = False) -> int:
+        return int(self.lib.oracle_key_to_ordered(int(bits) & (2**64 - 1), kind, int(descending)))
+
+    def ordered_to_key(self, u: int, kind: int, descending: bool = False) -> int:
+        return int(self.lib.oracle_ordered_to_key(int(u) & (2**64 - 1), kind, int(descending)))
+
+    def digit_histograms_general(self, keys, kind: int, begin_bit: int = 0,
+                                 end_bit: int | None = None, descending: bool = False):
+        k = _as_kind(keys, kind)
+        if end_bit is None:
+            end_bit = 8 * k.itemsize
+        p = (end_bit - begin_bit + 7) // 8
+        hist = np.zeros((max(p, 1), 256), dtype=np.uint32)
+        _check(self.lib.oracle_digit_histograms_general(
+            k.ctypes.data, k.size, kind, int(descending), begin_bit, end_bit, _ptr(hist)),
+            "digit_histograms_general")
+        return hist[:p]
+
+    def radix_sort(self, keys, vals=None, kind: int = 0, descending: bool = False,
+                   begin_bit: int = 0, end_bit: int | None = None):
+        """(keys_out with the input dtype, vals_out or None)."""
+        k = _as_kind(keys, kind)
+        if end_bit is None:
+            end_bit = 8 * k.itemsize
+        ko = np.empty_like(k)
+        v = vo = None
+        if vals is not None:
+            v = _as_u32(vals).ravel()
+            if v.size != k.size:
+                raise ValueError("keys and values differ in length")
+            vo = np.empty_like(v)
+        _check(self.lib.oracle_radix_sort_general(k.ctypes.data, _ptr(v), ko.ctypes.data, _ptr(vo),
+                                                  k.size, kind, int(descending), begin_bit,
+                                                  end_bit), "radix_sort_general")
+        return ko, vo
 
     # a4 -----------------------------------------------------------------
     def compact_positive(self, x):

@@ -70,12 +70,64 @@ def test_workspace_sizes(lib):
     assert lib.gsort_compact_workspace_bytes(1 << 30) == 0
 
 
+def test_general_workspace_sizes(lib):
+    HDR = 8192
+
+    def up(x):
+        return -(-x // 256) * 256
+    for n in (1, 4097, 1 << 20, (1 << 30) - 1):
+        tiles = (n + 4095) // 4096
+        state = 2 * up(tiles * 1024)
+        for kind in (0, 1, 2):     # 32-bit kinds: the same layout as gsort_radix_workspace_bytes
+            for wv in (0, 1):
+                assert lib.gsort_radix_sort_workspace_bytes(n, kind, wv) == \
+                    lib.gsort_radix_workspace_bytes(n, wv)
+        for kind in (3, 4, 5):     # 64-bit kinds: 8 KiB of histograms, 8-byte keys
+            assert lib.gsort_radix_sort_workspace_bytes(n, kind, 0) == HDR + 8192 + state + up(8 * n)
+            assert lib.gsort_radix_sort_workspace_bytes(n, kind, 1) == \
+                HDR + 8192 + state + up(8 * n) + up(4 * n)
+    assert lib.gsort_radix_sort_workspace_bytes(10, 6, 0) == 0
+    assert lib.gsort_radix_sort_workspace_bytes(10, -1, 0) == 0
+    assert lib.gsort_radix_sort_workspace_bytes(1 << 30, 3, 0) == 0
+
+
+def test_general_argument_errors(lib):
+    big = 1 << 40
+    f = lib.gsort_radix_sort
+    assert f(A, B, None, None, 0, 3, 1, 0, 64, None, 0, None) == 0            # n == 0: no-op
+    assert f(A, B, None, None, 10, 6, 0, 0, 32, W, big, None) == EINVAL        # no such kind
+    assert f(A, B, None, None, 10, 0, 2, 0, 32, W, big, None) == EINVAL        # unknown flag
+    assert f(A, B, None, None, 10, 2, 0, 0, 33, W, big, None) == EINVAL        # 32-bit kind, 33 bits
+    assert f(A, B, None, None, 10, 3, 0, 0, 65, W, big, None) == EINVAL
+    assert f(A + 4, B, None, None, 10, 3, 0, 0, 64, W, big, None) == EALIGN    # 64-bit keys: 8-byte aligned
+    assert f(A, B + 4, None, None, 10, 5, 0, 0, 64, W, big, None) == EALIGN
+    assert f(A, A + 8, None, None, 10, 3, 0, 0, 64, W, big, None) == EINVAL   # partial overlap (8-byte keys)
+    # output values must not fall inside the 8-byte keys (10 keys = 80 bytes)
+    assert f(A, B, B + 0x1000, A + 40, 10, 3, 0, 0, 64, W, big, None) == EINVAL
+    assert f(A, B, A + 0x1000, B + 72, 10, 3, 0, 0, 64, W, big, None) == EINVAL
+    assert f(A, B, None, None, 10, 3, 0, 0, 64, W, 100, None) == EWS
+    assert f(A, B, None, None, 10, 3, 0, 0, 64, None, big, None) == EWS
+    opt = __import__("bitonic_networks_gb300._lib", fromlist=["Options"]).Options(0, -1, None, 0, 1)
+    assert lib.gsort_radix_sort_ex(A, B, None, None, 10, 3, 0, 0, 64, W, big, None,
+                                   ctypes.byref(opt)) == EINVAL            # 64-bit keys: variant 0 only
+    # the 32-bit calls refuse 64-bit kinds
+    assert lib.gsort_radix_pairs(A, B, None, None, 10, 3, 0, 32, W, big, None) == EINVAL
+    assert lib.gsort_radix_keys(A, B, 10, 4, W, big, None) == EINVAL
+    h = lib.gsort_digit_histograms
+    assert h(A, 10, 3, 0, 65, B, None) == EINVAL
+    assert h(A + 4, 10, 3, 0, 64, B, None) == EALIGN
+    assert h(A, 10, 6, 0, 8, B, None) == EINVAL
+
+
 def test_launch_count(lib):
     assert lib.gsort_radix_launch_count(100, 0, 32, 0) == 6
     assert lib.gsort_radix_launch_count(100, 0, 8, 0) == 3
     assert lib.gsort_radix_launch_count(100, 0, 24, 1) == 6
     assert lib.gsort_radix_launch_count(0, 0, 32, 0) == 0
     assert lib.gsort_radix_launch_count(100, 5, 5, 0) == 0
+    assert lib.gsort_radix_sort_launch_count(100, 3, 0, 64, 0) == 11      # 2 + 8 passes + hist clear
+    assert lib.gsort_radix_sort_launch_count(100, 5, 0, 56, 1) == 11      # 7 passes, in place: + copy
+    assert lib.gsort_radix_sort_launch_count(100, 2, 0, 32, 0) == 6
 
 
 # Fake device addresses: validation rejects these calls before any CUDA call.
@@ -91,7 +143,7 @@ def test_radix_argument_errors(lib):
     assert f(A, B, None, None, 0, 0, 0, 32, None, 0, None) == 0          # n == 0: no-op
     assert f(A, B, None, None, -1, 0, 0, 32, W, big, None) == EINVAL
     assert f(A, B, None, None, 1 << 30, 0, 0, 32, W, big, None) == ETOOBIG
-    assert f(A, B, None, None, 10, 2, 0, 32, W, big, None) == EINVAL      # bad kind
+    assert f(A, B, None, None, 10, 6, 0, 32, W, big, None) == EINVAL      # bad kind
     assert f(A, B, None, None, 10, 0, 5, 4, W, big, None) == EINVAL       # begin > end
     assert f(A, B, None, None, 10, 0, 0, 33, W, big, None) == EINVAL
     assert f(A, B, None, None, 10, 0, -1, 8, W, big, None) == EINVAL

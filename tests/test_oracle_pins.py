@@ -378,12 +378,176 @@ def test_bitonic_padding(orc):
 
 # ------------------------------------------------------------ planted mistakes
 
+# --------------------------------------------- f1: every key kind, both directions
+
+import math
+
+KINDS = {"u32": 0, "f32": 1, "i32": 2, "u64": 3, "f64": 4, "i64": 5}
+KIND_DTYPE = {0: np.uint32, 1: np.float32, 2: np.int32, 3: np.uint64, 4: np.float64, 5: np.int64}
+
+
+def _py_key(kind):
+    """Python sort key of one numpy element: integer value, or (value, sign) for
+    floats so that -0.0 sorts before +0.0 (IEEE totalOrder on non-NaN values)."""
+    if kind in (1, 4):
+        return lambda v: (float(v), math.copysign(1.0, float(v)))
+    return lambda v: int(v)
+
+
+def _edge_keys(kind, n, seed):
+    rng = np.random.default_rng(seed)
+    dt = np.dtype(KIND_DTYPE[kind])
+    if kind in (1, 4):
+        vals = rng.standard_normal(n) * 10.0 ** rng.integers(-5, 6, n)
+        specials = [0.0, -0.0, np.inf, -np.inf, 1.0, -1.0, np.finfo(dt).tiny / 4,
+                    -np.finfo(dt).tiny / 4, np.finfo(dt).max, -np.finfo(dt).max]
+        vals[: len(specials)] = specials
+        vals = vals.astype(dt)
+        vals[rng.integers(0, n, n // 4)] = vals[rng.integers(0, n, n // 4)]   # duplicates
+    else:
+        info = np.iinfo(dt)
+        vals = rng.integers(info.min, info.max, n, dtype=dt, endpoint=True)
+        specials = [info.min, info.max, 0, 1]
+        if info.min < 0:
+            specials += [-1]
+        vals[: len(specials)] = np.array(specials, dtype=dt)
+        vals[rng.integers(0, n, n // 4)] = vals[rng.integers(0, n, n // 4)]
+    rng.shuffle(vals)
+    return vals
+
+
+def _python_stable(keys, kind, descending):
+    key = _py_key(kind)
+    order = sorted(range(len(keys)), key=lambda i: key(keys[i]), reverse=descending)
+    return np.array(order, dtype=np.uint32)
+
+
+def pin_general_vs_python_sorted(orc):
+    # Python's sorted() is stable, also with reverse=True (equal keys keep
+    # their input order), which is the order the descending sort promises.
+    for kind in range(6):
+        for desc in (False, True):
+            keys = _edge_keys(kind, 3000, 100 + kind)
+            idx = np.arange(keys.size, dtype=np.uint32)
+            ko, vo = orc.radix_sort(keys, idx, kind, desc)
+            exp = _python_stable(keys, kind, desc)
+            assert np.array_equal(vo, exp), (kind, desc)
+            assert np.array_equal(ko.view(np.uint8), keys[exp].view(np.uint8)), (kind, desc)
+
+
+def pin_general_bit_range(orc):
+    rng = np.random.default_rng(7)
+    keys = rng.integers(0, 2**64 - 1, 2000, dtype=np.uint64, endpoint=True)
+    keys[1::3] = keys[0::3][: keys[1::3].size]        # equal keys
+    idx = np.arange(keys.size, dtype=np.uint32)
+    for b, e in [(0, 64), (13, 51), (40, 64), (0, 9), (60, 61)]:
+        for desc in (False, True):
+            ko, vo = orc.radix_sort(keys, idx, 3, desc, b, e)
+            mask = (1 << (e - b)) - 1
+            exp = sorted(range(keys.size), key=lambda i: (int(keys[i]) >> b) & mask, reverse=desc)
+            assert vo.tolist() == exp, (b, e, desc)
+            assert np.array_equal(ko, keys[exp])
+
+
+def pin_general_bruteforce(orc, max_len=4):
+    alphabets = {
+        2: [-2**31, -1, 0, 1, 2**31 - 1],
+        3: [0, 1, 2**63, 2**64 - 1],
+        4: [-np.inf, -1.0, -0.0, 0.0, 1.0, np.inf],
+        5: [-2**63, -1, 0, 2**63 - 1],
+    }
+    for kind, alpha in alphabets.items():
+        dt = KIND_DTYPE[kind]
+        key = _py_key(kind)
+        for length in range(1, max_len + 1):
+            for combo in itertools.product(range(len(alpha)), repeat=length):
+                keys = np.array([alpha[c] for c in combo], dtype=dt)
+                idx = np.arange(length, dtype=np.uint32)
+                for desc in (False, True):
+                    ko, vo = orc.radix_sort(keys, idx, kind, desc)
+                    assert sorted(vo.tolist()) == list(range(length))        # a permutation
+                    assert np.array_equal(ko.view(np.uint8), keys[vo].view(np.uint8))
+                    ks = [key(v) for v in ko]
+                    for i in range(length - 1):
+                        if desc:
+                            assert ks[i] >= ks[i + 1]
+                        else:
+                            assert ks[i] <= ks[i + 1]
+                        if ks[i] == ks[i + 1]:
+                            assert vo[i] < vo[i + 1]                        # stable
+
+
+def pin_general_maps(orc):
+    rng = np.random.default_rng(11)
+    for kind in range(6):
+        w = 8 * np.dtype(KIND_DTYPE[kind]).itemsize
+        bits = [int(x) for x in rng.integers(0, 2**w - 1, 400, dtype=np.uint64, endpoint=True)]
+        for desc in (False, True):
+            for b in bits:                                   # the map is a bijection on bit patterns
+                u = orc.key_to_ordered(b, kind, desc)
+                assert 0 <= u < 2**w
+                assert orc.ordered_to_key(u, kind, desc) == b
+        # monotone along values sorted by Python
+        keys = _edge_keys(kind, 500, 200 + kind)
+        if kind in (1, 4):
+            keys = keys[~np.isnan(keys)]
+        key = _py_key(kind)
+        ordered = sorted(keys.tolist(), key=key)
+        as_bits = np.array(ordered, dtype=KIND_DTYPE[kind]).view(np.uint32 if w == 32 else np.uint64)
+        us = [orc.key_to_ordered(int(b), kind) for b in as_bits]
+        ud = [orc.key_to_ordered(int(b), kind, True) for b in as_bits]
+        for i in range(len(us) - 1):
+            same = key(ordered[i]) == key(ordered[i + 1])
+            assert (us[i] == us[i + 1]) if same else (us[i] < us[i + 1])
+            assert (ud[i] == ud[i + 1]) if same else (ud[i] > ud[i + 1])
+
+
+def pin_general_histograms(orc):
+    keys = _edge_keys(5, 3000, 5)
+    h = orc.digit_histograms_general(keys, 5)
+    assert h.shape == (8, 256) and (h.sum(axis=1) == keys.size).all()
+    u = np.array([orc.key_to_ordered(int(b), 5) for b in keys.view(np.uint64)], dtype=np.uint64)
+    for p in range(8):
+        assert np.array_equal(h[p], np.bincount(((u >> np.uint64(8 * p)) & np.uint64(255)).astype(np.int64),
+                                                minlength=256))
+
+
+def test_general_vs_python_sorted(orc):
+    pin_general_vs_python_sorted(orc)
+
+
+def test_general_bit_range(orc):
+    pin_general_bit_range(orc)
+
+
+def test_general_bruteforce(orc):
+    pin_general_bruteforce(orc)
+
+
+def test_general_maps(orc):
+    pin_general_maps(orc)
+
+
+def test_general_histograms(orc):
+    pin_general_histograms(orc)
+
+
+def test_general_matches_32bit_oracle(orc):
+    # the two oracle entry points agree on the kinds they share
+    keys = synth.uniform_keys(5000, 3)
+    idx = np.arange(5000, dtype=np.uint32)
+    a = orc.radix_sort_pairs(keys, idx, 0, 3, 29)
+    b = orc.radix_sort(keys, idx, 0, False, 3, 29)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
 MUTANTS = {
     # a reversed scatter: each pass is no longer stable
     "unstable_scatter": ("for (int64_t i = 0; i < n; ++i) {\n            uint32_t d = digit_of",
                          "for (int64_t i = n - 1; i >= 0; --i) {\n            uint32_t d = digit_of"),
     # digits taken 7 bits apart instead of 8
-    "digit_stride": ("int lo = begin_bit + 8 * p;", "int lo = begin_bit + 7 * p;"),
+    "digit_stride": ("digit_of(uint32_t k, int begin_bit, int end_bit, int p)\n{\n    int lo = begin_bit + 8 * p;",
+                     "digit_of(uint32_t k, int begin_bit, int end_bit, int p)\n{\n    int lo = begin_bit + 7 * p;"),
     # the integer sign trick applied to floats (negatives not reversed)
     "float_map_sign_only": ("        return ~bits;\n    return bits | 0x80000000u;",
                             "        return bits ^ 0x80000000u;\n    return bits | 0x80000000u;"),
@@ -392,13 +556,30 @@ MUTANTS = {
     # bitonic direction from the wrong bit
     "bitonic_direction": ("int ascending = (i & k) == 0;", "int ascending = (i & j) == 0;"),
     # last digit not narrowed to the remaining bits
-    "last_digit_width": ("    if (width > 8)\n        width = 8;", "    width = 8;"),
+    "last_digit_width": ("int lo = begin_bit + 8 * p;\n    int width = end_bit - lo;\n    if (width > 8)\n        width = 8;\n    return (uint32_t)(((uint64_t)k",
+                         "int lo = begin_bit + 8 * p;\n    int width = end_bit - lo;\n    width = 8;\n    return (uint32_t)(((uint64_t)k"),
+    # f1: reversed scatter in the general sort (not stable)
+    "general_unstable": ("for (int64_t i = 0; i < n; ++i) {\n            uint32_t slot = next[digit_of64",
+                         "for (int64_t i = n - 1; i >= 0; --i) {\n            uint32_t slot = next[digit_of64"),
+    # f1: 64-bit digits 7 bits apart
+    "digit64_stride": ("digit_of64(uint64_t k, int begin_bit, int end_bit, int p)\n{\n    int lo = begin_bit + 8 * p;",
+                       "digit_of64(uint64_t k, int begin_bit, int end_bit, int p)\n{\n    int lo = begin_bit + 7 * p;"),
+    # f1: signed 64-bit offset by 2^62 instead of 2^63
+    "i64_offset": ("case 5: u = bits + 0x8000000000000000ull; break;",
+                   "case 5: u = bits + 0x4000000000000000ull; break;"),
+    # f1: negative doubles only get the sign bit flipped
+    "f64_sign_only": ("        if (bits >> 63)\n            u = ~bits;",
+                      "        if (bits >> 63)\n            u = bits ^ 0x8000000000000000ull;"),
+    # f1: descending complement at 32 bits for every width
+    "descending_width": ("    }\n    if (descending)\n        u = (w == 64 ? 0xFFFFFFFFFFFFFFFFull : 0xFFFFFFFFull) - u;",
+                         "    }\n    if (descending)\n        u = 0xFFFFFFFFull - u;"),
 }
 
 PINS = [pin_radix_worked_example, pin_compaction_worked_example, pin_bitonic_exercise,
         pin_transform_matches_float_compare, pin_histograms_constructed,
         pin_sort_vs_python_sorted, pin_float_sort_vs_python_sorted,
-        pin_compaction_specials, pin_bitonic_zero_one, pin_segmented_vs_numpy]
+        pin_compaction_specials, pin_bitonic_zero_one, pin_segmented_vs_numpy,
+        pin_general_vs_python_sorted, pin_general_bit_range, pin_general_maps]
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
