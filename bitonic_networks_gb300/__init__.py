@@ -8,9 +8,10 @@ to reach the input generators in `synth`) does not require the CUDA library.
 import importlib
 
 __all__ = [
-    "sort", "sort_keys", "sort_pairs", "compact_positive", "segmented_sort_",
+    "sort", "sort_keys", "sort_pairs", "compact_positive", "segmented_sort_", "segmented_sort",
     "digit_histograms", "GsortError", "library_path",
-    "radix_workspace_bytes", "sort_workspace_bytes", "compact_workspace_bytes",
+    "radix_workspace_bytes", "sort_workspace_bytes", "segmented_sort_workspace_bytes",
+    "compact_workspace_bytes",
 ]
 
 

@@ -75,6 +75,17 @@ SIGNATURES = {
                                                       ctypes.c_void_p]),
     "gsort_segmented_bitonic": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
                                                ctypes.c_void_p]),
+    "gsort_segmented_sort_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64,
+                                                               ctypes.c_int]),
+    "gsort_segmented_sort": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                            ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                                            ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "gsort_segmented_sort_ex": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                               ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                                               ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                               ctypes.POINTER(Options)]),
     "gsort_check": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "gsort_radix_num_variants": (ctypes.c_int, []),
     "gsort_radix_variant_name": (ctypes.c_char_p, [ctypes.c_int]),

@@ -278,6 +278,77 @@ int gsort_check(const void *d_ws, cudaStream_t stream) {
     return static_cast<int>(status);
 }
 
+size_t gsort_segmented_sort_workspace_bytes(int64_t n, int64_t num_segments, int with_values) {
+    if (n < 0 || n > GSORT_MAX_N || num_segments < 0 || num_segments > GSORT_MAX_N) return 0;
+    return seg_layout(static_cast<uint32_t>(n), static_cast<uint32_t>(num_segments), with_values != 0)
+        .total;
+}
+
+int gsort_segmented_sort_ex(const void *d_keys_in, void *d_keys_out, const uint32_t *d_vals_in,
+                            uint32_t *d_vals_out, int64_t n, const uint32_t *d_offsets,
+                            int64_t num_segments, int kind, int flags, void *d_ws, size_t ws_bytes,
+                            cudaStream_t stream, const gsort_options *options) {
+    const gsort_options *o = options ? options : &kDefaults;
+    if (n < 0 || num_segments < 0) return GSORT_EINVAL;
+    if (n > GSORT_MAX_N || num_segments > GSORT_MAX_N) return GSORT_ETOOBIG;
+    if (key_kind_bytes(kind) != 4) return GSORT_EINVAL;
+    if ((flags & ~GSORT_DESCENDING) != 0) return GSORT_EINVAL;
+    if ((d_vals_in == nullptr) != (d_vals_out == nullptr)) return GSORT_EINVAL;
+    if (o->num_events < 0 || (o->num_events > 0 && o->events == nullptr)) return GSORT_EINVAL;
+    if (n == 0) return GSORT_OK;
+    if (num_segments == 0) return GSORT_EINVAL;   // n > 0 keys need at least one segment
+    if (d_keys_in == nullptr || d_keys_out == nullptr || d_offsets == nullptr) return GSORT_EINVAL;
+    if (!aligned(d_keys_in, 4) || !aligned(d_keys_out, 4) || !aligned(d_offsets, 4)) return GSORT_EALIGN;
+    if (d_vals_in != nullptr && (!aligned(d_vals_in, 4) || !aligned(d_vals_out, 4))) return GSORT_EALIGN;
+    const bool pairs = d_vals_in != nullptr;
+    const size_t bytes = static_cast<size_t>(n) * 4;
+    const size_t obytes = (static_cast<size_t>(num_segments) + 1) * 4;
+    if (partial_overlap(d_keys_in, d_keys_out, bytes)) return GSORT_EINVAL;
+    if (ranges_overlap(d_offsets, obytes, d_keys_out, bytes)) return GSORT_EINVAL;
+    if (pairs) {
+        if (partial_overlap(d_vals_in, d_vals_out, bytes)) return GSORT_EINVAL;
+        if (overlap(d_keys_out, d_vals_out, bytes) || overlap(d_keys_in, d_vals_out, bytes) ||
+            overlap(d_keys_out, d_vals_in, bytes) || ranges_overlap(d_offsets, obytes, d_vals_out, bytes))
+            return GSORT_EINVAL;
+    }
+    if (d_ws == nullptr) return GSORT_EWORKSPACE;
+    if (!aligned(d_ws, kWsAlign)) return GSORT_EALIGN;
+    const SegLayout lay = seg_layout(static_cast<uint32_t>(n), static_cast<uint32_t>(num_segments), pairs);
+    if (ws_bytes < lay.total) return GSORT_EWORKSPACE;
+    if (ranges_overlap(d_ws, ws_bytes, d_keys_in, bytes) || ranges_overlap(d_ws, ws_bytes, d_keys_out, bytes) ||
+        ranges_overlap(d_ws, ws_bytes, d_offsets, obytes) ||
+        (pairs && (ranges_overlap(d_ws, ws_bytes, d_vals_in, bytes) ||
+                   ranges_overlap(d_ws, ws_bytes, d_vals_out, bytes))))
+        return GSORT_EINVAL;
+    DeviceInfo dev;
+    if (device_info(&dev) != GSORT_OK) return GSORT_ECUDA;
+    SegLaunch L;
+    L.keys_in = static_cast<const uint32_t *>(d_keys_in);
+    L.keys_out = static_cast<uint32_t *>(d_keys_out);
+    L.vals_in = d_vals_in;
+    L.vals_out = d_vals_out;
+    L.n = static_cast<uint32_t>(n);
+    L.offsets = d_offsets;
+    L.num_segments = static_cast<uint32_t>(num_segments);
+    L.kind = kind;
+    L.flags = flags;
+    L.ws = static_cast<unsigned char *>(d_ws);
+    L.spin_limit = o->spin_limit ? o->spin_limit : kDefaultSpinLimit;
+    L.events = reinterpret_cast<cudaEvent_t *>(o->events);
+    L.num_events = o->num_events;
+    L.stream = stream;
+    L.sm_count = dev.sm_count;
+    return launch_segmented_sort(L);
+}
+
+int gsort_segmented_sort(const void *d_keys_in, void *d_keys_out, const uint32_t *d_vals_in,
+                         uint32_t *d_vals_out, int64_t n, const uint32_t *d_offsets,
+                         int64_t num_segments, int kind, int flags, void *d_ws, size_t ws_bytes,
+                         cudaStream_t stream) {
+    return gsort_segmented_sort_ex(d_keys_in, d_keys_out, d_vals_in, d_vals_out, n, d_offsets,
+                                   num_segments, kind, flags, d_ws, ws_bytes, stream, nullptr);
+}
+
 int gsort_radix_num_variants(void) { return radix_num_variants(); }
 
 const char *gsort_radix_variant_name(int variant) { return radix_variant_name(variant); }

@@ -235,4 +235,32 @@ int launch_compact(const CompactLaunch &L);
 int launch_segmented_bitonic(uint32_t *keys, int64_t num_segments, int segment_len,
                              cudaStream_t stream);
 
+// Variable-length segmented sort (segsort.cu): workspace layout and launch.
+struct SegLayout {
+    uint32_t small_max;   // segments of 2..1024 keys, at most
+    uint32_t large_max;   // segments of more than 1024 keys, at most
+    uint32_t tiles_max;   // tiles of the large segments, at most
+    size_t small_list, large_start, large_len, tile_base, tiles, hist, look_a, look_b;
+    size_t tmp_keys, tmp_vals, total;
+};
+SegLayout seg_layout(uint32_t n, uint32_t num_segments, bool with_values);
+
+struct SegLaunch {
+    const uint32_t *keys_in;
+    uint32_t *keys_out;
+    const uint32_t *vals_in;   // null: keys only
+    uint32_t *vals_out;
+    uint32_t n;
+    const uint32_t *offsets;   // num_segments + 1 entries
+    uint32_t num_segments;
+    int kind, flags;
+    unsigned char *ws;
+    uint32_t spin_limit;
+    cudaEvent_t *events;
+    int num_events;
+    cudaStream_t stream;
+    int sm_count;
+};
+int launch_segmented_sort(const SegLaunch &L);
+
 }  // namespace gsort

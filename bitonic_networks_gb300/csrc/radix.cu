@@ -101,11 +101,12 @@ __global__ void __launch_bounds__(WARPS * 32, 2) k_digit_pass_persistent(const P
         }
         phase[b] ^= 1u;
         const ClaimNext<TILE, PAIRS> claim{&prefetch, a.tile_counter, &s_misc[24], tiles, b ^ 1u};
+        const TileDesc td{tile, 0u, tile_n, a.hist, 0u, a.n};
         bool ok;
         if (tile_n == static_cast<uint32_t>(TILE))
-            ok = pass_tile<uint32_t, WARPS, IPT, MATCH, LW, BYTE, PAIRS, XIN, XOUT, true>(a, tab, tile, kb, vb, kb, vb, claim);
+            ok = pass_tile<uint32_t, WARPS, IPT, MATCH, LW, BYTE, PAIRS, XIN, XOUT, true>(a, tab, td, kb, vb, kb, vb, claim);
         else
-            ok = pass_tile<uint32_t, WARPS, IPT, MATCH, LW, BYTE, PAIRS, XIN, XOUT, false>(a, tab, tile, kb, vb, kb, vb, claim);
+            ok = pass_tile<uint32_t, WARPS, IPT, MATCH, LW, BYTE, PAIRS, XIN, XOUT, false>(a, tab, td, kb, vb, kb, vb, claim);
         __syncthreads();   // buffer b is read out, and the next tile id is visible
         const uint32_t next = s_misc[24];
         if (!ok && tile != a.stall_tile) {   // a look-back gave up

@@ -320,23 +320,36 @@ __host__ __device__ constexpr size_t pass_smem_words() {
            256 + 32;
 }
 
-// Exclusive prefix of digit d over all tiles before `tile`.  Each word holds a
-// flag (AGG: the tile's count; PREFIX: the count over tiles 0..t) and a
-// 30-bit count, so one round trip reads W predecessors at once; the
-// nearest PREFIX word ends the walk and the AGG words before it are summed.
-// Returns false if a wait gave up.
+// Where one tile sits: its look-back row, the first row of its chain (the
+// tiles first..row share one prefix: the whole input, or one segment), its
+// keys, the 256 counts of the pass for its chain, and the output range.
+struct TileDesc {
+    uint32_t row;           // look-back row of this tile
+    uint32_t first;         // look-back row of the chain's first tile
+    uint32_t n;             // keys in this tile
+    const uint32_t *hist;   // the chain's 256 digit counts of this pass
+    uint32_t out_base;      // output index of the chain's first key
+    uint32_t out_end;       // one past the chain's last output index
+};
+
+// Exclusive prefix of digit d over the tiles first .. row-1 of the chain.
+// Each word holds a flag (AGG: the tile's count; PREFIX: the count over the
+// chain's tiles up to this one) and a 30-bit count, so one round trip reads W
+// predecessors at once; the nearest PREFIX word ends the walk and the AGG
+// words before it are summed.  Returns false if a wait gave up.
 template <int W>
-__device__ __forceinline__ bool look_back(const PassArgs &a, uint32_t tile, uint32_t d,
+__device__ __forceinline__ bool look_back(const PassArgs &a, const TileDesc &td, uint32_t d,
                                           uint32_t &excl) {
     excl = 0;
-    int32_t t = static_cast<int32_t>(tile) - 1;
+    int32_t t = static_cast<int32_t>(td.row) - 1;
+    const int32_t first = static_cast<int32_t>(td.first);
     uint32_t polls = 0, ns = 32;
     while (true) {
         uint32_t w[W];
 #pragma unroll
         for (int i = 0; i < W; ++i)
-            w[i] = (t - i >= 0) ? ld_relaxed(a.look + static_cast<uint32_t>(t - i) * 256 + d)
-                                : kFlagPrefix;   // before tile 0: an empty prefix
+            w[i] = (t - i >= first) ? ld_relaxed(a.look + static_cast<uint32_t>(t - i) * 256 + d)
+                                    : kFlagPrefix;   // before the chain: an empty prefix
         // sum words up to and including the nearest PREFIX; any empty word
         // before it means a predecessor has not published yet
         uint32_t sum = 0;
@@ -373,7 +386,7 @@ struct NoHook {
 
 template <class K, int WARPS, int IPT, int MATCH, int LW, bool BYTE, bool PAIRS, bool XIN, bool XOUT,
           bool FULL, class Hook = NoHook>
-__device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, uint32_t tile,
+__device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, const TileDesc &td,
                                           const K *kin, const uint32_t *vin,
                                           K *s_keys, uint32_t *s_vals,
                                           const Hook &before_output = Hook()) {
@@ -384,8 +397,8 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, uint
     uint32_t *s_misc = s_goff + 256;            // [32]
 
     const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint32_t tile_base = tile * TILE;
-    const uint32_t tile_n = FULL ? TILE : a.n - tile_base;
+    const uint32_t tile = td.row;
+    const uint32_t tile_n = FULL ? TILE : td.n;
     // Item k of this thread sits at tile index item0 + 32k: each warp owns a
     // contiguous run of 32*IPT keys and walks it in order, which makes the
     // warp-local ranks stable.
@@ -425,8 +438,8 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, uint
             cnt += cw;
         }
         if (tile != a.stall_tile)
-            st_relaxed(a.look + tile * 256 + tid, (tile == 0 ? kFlagPrefix : kFlagAgg) | cnt);
-        const uint32_t bin = a.hist[tid];
+            st_relaxed(a.look + tile * 256 + tid, (tile == td.first ? kFlagPrefix : kFlagAgg) | cnt);
+        const uint32_t bin = td.hist[tid];
         const uint32_t ic = warp_inclusive_scan(cnt, lane);
         const uint32_t ib = warp_inclusive_scan(bin, lane);
         if (lane == 31) {
@@ -455,8 +468,8 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, uint
     if (tid < 256) {
         uint32_t excl = 0;
         bool ok = true;
-        if (tile > 0 && tile != a.stall_tile) {
-            ok = look_back<LW>(a, tile, tid, excl);
+        if (tile > td.first && tile != a.stall_tile) {
+            ok = look_back<LW>(a, td, tid, excl);
             if (ok) st_relaxed(a.look + tile * 256 + tid, kFlagPrefix | (excl + cnt));
         }
         if (!ok) {
@@ -464,7 +477,7 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, uint
             record_error(a.status, a.abort_flag, GSORT_ETIMEOUT);
         }
         // global index of tile slot i holding digit d: s_goff[d] + i
-        s_goff[tid] = bin_excl + excl - tile_excl;
+        s_goff[tid] = td.out_base + bin_excl + excl - tile_excl;
     }
 
     // ---- warp multisplit: stable slot of each key in the tile-sorted order
@@ -502,7 +515,7 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, uint
         if (FULL || i < tile_n) {
             const K kk = s_keys[i];
             const uint32_t g = s_goff[digit_at<BYTE>(kk, a.shift, a.mask)] + i;
-            if (g < a.n) {
+            if (g < td.out_end) {
                 dst_k[g] = XOUT ? order_out<K>(kk, static_cast<K>(a.fmask), static_cast<K>(a.flip)) : kk;
                 if (PAIRS) a.dst_v[g] = s_vals[i];
             }
@@ -533,10 +546,11 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass(const PassArgs 
     uint32_t *s_vals = smem + TILE * kKeyWords;
     const K *kin = static_cast<const K *>(a.src_k) + tile * TILE;
     const uint32_t *vin = PAIRS ? a.src_v + tile * TILE : nullptr;
-    if (a.n - tile * TILE >= static_cast<uint32_t>(TILE))
-        pass_tile<K, WARPS, IPT, MATCH, LW, BYTE, PAIRS, XIN, XOUT, true>(a, s_cnt, tile, kin, vin, s_keys, s_vals);
+    const TileDesc td{tile, 0u, min(static_cast<uint32_t>(TILE), a.n - tile * TILE), a.hist, 0u, a.n};
+    if (td.n == static_cast<uint32_t>(TILE))
+        pass_tile<K, WARPS, IPT, MATCH, LW, BYTE, PAIRS, XIN, XOUT, true>(a, s_cnt, td, kin, vin, s_keys, s_vals);
     else
-        pass_tile<K, WARPS, IPT, MATCH, LW, BYTE, PAIRS, XIN, XOUT, false>(a, s_cnt, tile, kin, vin, s_keys, s_vals);
+        pass_tile<K, WARPS, IPT, MATCH, LW, BYTE, PAIRS, XIN, XOUT, false>(a, s_cnt, td, kin, vin, s_keys, s_vals);
 }
 
 // One-tile-per-CTA launch configuration of the digit pass.

@@ -1,0 +1,509 @@
+// segsort.cu -- stable sort of variable-length segments (an offsets array),
+// the hybrid strategy of [PMPP10] 10.5 (strategy 2: radix sort for the
+// coarse order, bitonic networks for small pieces) and of [GPUSORT]
+// (partitioned sort whose pieces of <= 1024 keys go to a bitonic sort):
+//
+//   classify   one pass over the segments: checks the offsets, lists the
+//              segments of 2..1024 keys ("small") and of more than 1024 keys
+//              ("large"), copies segments of one key when the output is
+//              another buffer
+//   scan       exclusive scan of the tile counts of the large segments: the
+//              tiles of segment j are rows tile_base[j] .. tile_base[j+1]-1
+//   tilemap    one descriptor per tile: its segment, keys, look-back chain
+//   histogram  the 4 x 256 digit counts of every large segment
+//   4 x pass   the single-pass digit scatter of radix_kernels.cuh on tiles
+//              that never straddle a segment: bin starts come from the
+//              segment's own histogram, and the decoupled look-back of a tile
+//              stops at its segment's first tile (a chain per segment)
+//   small      one warp per small segment: the register bitonic network of
+//              bitonic_network.cuh; with values, the network sorts (key,
+//              position) composites, which makes the result stable
+//
+// Every segment is sorted by the whole mapped key (the order map of the key
+// kind and direction, as in the radix sort), equal keys keeping their input
+// order, so the result is unique with or without values.
+#include "bitonic_network.cuh"
+#include "radix_kernels.cuh"
+
+namespace gsort {
+namespace {
+
+constexpr uint32_t kSmallMax = 1024;                  // longest segment the warp network takes
+constexpr int kSegPassWarps = 16, kSegPassIpt = 16;
+constexpr uint32_t kSegTile = kSegPassWarps * 32 * kSegPassIpt;   // 8192 keys
+constexpr int kSmallWarps = 4;
+
+// Header words (after the tile counters): list lengths and the tile total.
+constexpr size_t kHdrSegCounts = kHdrHist;   // u32 [0] small, [1] large, [2] tiles
+
+// Descriptor of one tile of a large segment (32 bytes: two 16-byte loads).
+struct SegTile {
+    uint32_t seg;        // index into the large-segment arrays
+    uint32_t base;       // index of the tile's first key
+    uint32_t n;          // keys in the tile
+    uint32_t first;      // look-back row of the segment's first tile
+    uint32_t out_base;   // the segment's first index
+    uint32_t out_end;    // one past the segment's last index
+    uint32_t pad[2];
+};
+
+// ---------------------------------------------------------------- classify
+__global__ void k_seg_classify(const uint32_t *__restrict__ offsets, uint32_t num_segments,
+                               uint32_t n, uint32_t *small_list, uint32_t small_max,
+                               uint32_t *large_start, uint32_t *large_len, uint32_t large_max,
+                               uint4 *hist, const uint32_t *keys_in, uint32_t *keys_out,
+                               const uint32_t *vals_in, uint32_t *vals_out, uint32_t *counts,
+                               uint32_t *status, uint32_t *abort_flag) {
+    for (uint32_t s = blockIdx.x * blockDim.x + threadIdx.x; s < num_segments;
+         s += gridDim.x * blockDim.x) {
+        const uint32_t a = offsets[s], b = offsets[s + 1];
+        const bool bad = b < a || b > n || (s == 0 && a != 0) || (s == num_segments - 1 && b != n);
+        if (bad) {
+            record_error(status, abort_flag, GSORT_EINVAL);
+            continue;
+        }
+        const uint32_t len = b - a;
+        if (len > kSmallMax) {
+            const uint32_t j = atomicAdd(&counts[1], 1u);
+            if (j >= large_max) {   // only reachable with overlapping (invalid) segments
+                record_error(status, abort_flag, GSORT_EINVAL);
+                continue;
+            }
+            large_start[j] = a;
+            large_len[j] = len;
+            for (uint32_t i = 0; i < 256; ++i) hist[j * 256 + i] = make_uint4(0, 0, 0, 0);
+        } else if (len >= 2) {
+            const uint32_t j = atomicAdd(&counts[0], 1u);
+            if (j >= small_max) {
+                record_error(status, abort_flag, GSORT_EINVAL);
+                continue;
+            }
+            small_list[j] = s;
+        } else if (len == 1 && keys_out != keys_in) {
+            keys_out[a] = keys_in[a];
+            if (vals_out != nullptr) vals_out[a] = vals_in[a];
+        } else if (len == 1 && vals_out != nullptr && vals_out != vals_in) {
+            vals_out[a] = vals_in[a];
+        }
+    }
+}
+
+// -------------------------------------------------------------------- scan
+// One CTA: exclusive scan of ceil(len / tile) over the large segments; each
+// thread scans a contiguous chunk, the chunk totals are scanned across the CTA.
+constexpr int kScanThreads = 1024;
+
+__global__ void __launch_bounds__(kScanThreads)
+k_seg_scan(const uint32_t *large_len, uint32_t large_max, uint32_t tiles_max, uint32_t *tile_base,
+           uint32_t *counts, uint32_t *status, uint32_t *abort_flag) {
+    __shared__ uint32_t s_warp[32];
+    __shared__ uint32_t s_total;
+    const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool aborted = ld_relaxed(abort_flag) != 0;
+    const uint32_t L = aborted ? 0u : min(counts[1], large_max);
+    const uint32_t chunk = (L + kScanThreads - 1) / kScanThreads;
+    const uint32_t lo = min(L, tid * chunk), hi = min(L, lo + chunk);
+    uint32_t sum = 0;
+    for (uint32_t j = lo; j < hi; ++j) sum += (large_len[j] + kSegTile - 1) / kSegTile;
+    const uint32_t inc = warp_inclusive_scan(sum, lane);
+    if (lane == 31) s_warp[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t w = s_warp[lane];
+        const uint32_t wi = warp_inclusive_scan(w, lane);
+        s_warp[lane] = wi - w;
+        if (lane == 31) s_total = wi;
+    }
+    __syncthreads();
+    uint32_t run = s_warp[warp] + inc - sum;
+    for (uint32_t j = lo; j < hi; ++j) {
+        tile_base[j] = run;
+        run += (large_len[j] + kSegTile - 1) / kSegTile;
+    }
+    if (tid == 0) {
+        uint32_t total = s_total;
+        if (total > tiles_max) {   // only reachable with overlapping (invalid) segments
+            record_error(status, abort_flag, GSORT_EINVAL);
+            total = 0;
+        }
+        tile_base[L] = total;
+        counts[2] = total;
+    }
+}
+
+// ----------------------------------------------------------------- tilemap
+// One warp per large segment writes the descriptors of its tiles.
+__global__ void k_seg_tilemap(const uint32_t *large_start, const uint32_t *large_len,
+                              const uint32_t *tile_base, const uint32_t *counts, uint32_t large_max,
+                              SegTile *tiles, const uint32_t *abort_flag) {
+    if (ld_relaxed(abort_flag)) return;
+    const uint32_t L = min(counts[1], large_max);
+    const uint32_t lane = threadIdx.x & 31;
+    const uint32_t warps = gridDim.x * (blockDim.x >> 5);
+    for (uint32_t j = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); j < L; j += warps) {
+        const uint32_t a = large_start[j], len = large_len[j], first = tile_base[j];
+        const uint32_t nt = (len + kSegTile - 1) / kSegTile;
+        for (uint32_t k = lane; k < nt; k += 32) {
+            SegTile t;
+            t.seg = j;
+            t.base = a + k * kSegTile;
+            t.n = min(kSegTile, len - k * kSegTile);
+            t.first = first;
+            t.out_base = a;
+            t.out_end = a + len;
+            t.pad[0] = t.pad[1] = 0;
+            tiles[first + k] = t;
+        }
+    }
+}
+
+// --------------------------------------------------------------- histogram
+// Grid-stride over tiles; each tile counts the four digits of its mapped
+// keys in shared memory and adds the counts to its segment's histogram.  It
+// also clears its look-back row of the first pass.
+template <bool XF>
+__global__ void __launch_bounds__(256)
+k_seg_hist(const uint32_t *__restrict__ keys, const SegTile *tiles, const uint32_t *counts,
+           uint32_t fmask, uint32_t flip, uint32_t *hist, uint32_t *look_clear,
+           const uint32_t *abort_flag) {
+    __shared__ uint32_t s_h[4 * 256];
+    if (ld_relaxed(abort_flag)) return;
+    const uint32_t total = counts[2];
+    const uint32_t tid = threadIdx.x;
+    for (uint32_t t = blockIdx.x; t < total; t += gridDim.x) {
+        const SegTile d = tiles[t];
+        for (uint32_t i = tid; i < 4 * 256; i += 256) s_h[i] = 0;
+        for (uint32_t i = tid; i < 256; i += 256) look_clear[t * 256 + i] = 0;
+        __syncthreads();
+        for (uint32_t i = tid; i < d.n; i += 256) {
+            uint32_t k = keys[d.base + i];
+            if (XF) k = order_in<uint32_t>(k, fmask, flip);
+#pragma unroll
+            for (int p = 0; p < 4; ++p) atomicAdd(&s_h[p * 256 + ((k >> (8 * p)) & 0xFFu)], 1u);
+        }
+        __syncthreads();
+        for (uint32_t i = tid; i < 4 * 256; i += 256)
+            if (s_h[i]) atomicAdd(&hist[d.seg * 1024 + i], s_h[i]);
+        __syncthreads();
+    }
+}
+
+// -------------------------------------------------------------------- pass
+// Persistent CTAs claim tiles in increasing order (a CTA finishes one tile
+// before it claims the next), so the smallest unfinished tile can always
+// complete its look-back, whose chain ends at its segment's first tile.
+template <bool BYTE, bool PAIRS, bool XIN, bool XOUT>
+__global__ void __launch_bounds__(kSegPassWarps * 32, 2)
+k_seg_pass(const PassArgs a, const SegTile *tiles, const uint32_t *counts, const uint32_t *hist) {
+    constexpr int T = kSegPassWarps * 32;
+    constexpr int TILE = kSegTile;
+    extern __shared__ __align__(128) uint32_t smem[];
+    uint32_t *s_keys = smem;
+    uint32_t *s_vals = smem + TILE;
+    uint32_t *s_cnt = smem + TILE * (PAIRS ? 2 : 1);
+    uint32_t *s_misc = s_cnt + kSegPassWarps * kRow + 256;
+    const uint32_t tid = threadIdx.x;
+    const uint32_t total = counts[2];
+    while (true) {
+        if (tid == 0) {
+            s_misc[0] = atomicAdd(a.tile_counter, 1u);
+            s_misc[1] = ld_relaxed(a.abort_flag);
+            s_misc[2] = 0;
+        }
+        for (uint32_t i = tid; i < kSegPassWarps * kRow; i += T) s_cnt[i] = 0;
+        __syncthreads();
+        const uint32_t t = s_misc[0];
+        if (s_misc[1] || t >= total) return;   // uniform: every thread read the same words
+        const SegTile d = tiles[t];
+        const TileDesc td{t, d.first, d.n, hist + d.seg * 1024 + (a.shift / 8) * 256, d.out_base,
+                          d.out_end};
+        const uint32_t *kin = static_cast<const uint32_t *>(a.src_k) + d.base;
+        const uint32_t *vin = PAIRS ? a.src_v + d.base : nullptr;
+        bool ok;
+        if (d.n == static_cast<uint32_t>(TILE))
+            ok = pass_tile<uint32_t, kSegPassWarps, kSegPassIpt, kMatchTable, 8, BYTE, PAIRS, XIN, XOUT, true>(
+                a, s_cnt, td, kin, vin, s_keys, s_vals);
+        else
+            ok = pass_tile<uint32_t, kSegPassWarps, kSegPassIpt, kMatchTable, 8, BYTE, PAIRS, XIN, XOUT, false>(
+                a, s_cnt, td, kin, vin, s_keys, s_vals);
+        if (!ok) return;   // a look-back gave up (the abort flag is raised)
+        __syncthreads();   // the tile buffers are read out before the next tile reuses them
+    }
+}
+
+template <bool PAIRS>
+struct SegPassLaunch {
+    template <bool XI, bool XO>
+    static cudaError_t one(const PassArgs &a, const SegTile *tiles, const uint32_t *counts,
+                           const uint32_t *hist, uint32_t grid, cudaStream_t s) {
+        auto k = k_seg_pass<true, PAIRS, XI, XO>;
+        const size_t smem = (static_cast<size_t>(kSegTile) * (PAIRS ? 2 : 1) + kSegPassWarps * kRow +
+                             256 + 32) * sizeof(uint32_t);
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        k<<<grid, kSegPassWarps * 32, smem, s>>>(a, tiles, counts, hist);
+        return cudaGetLastError();
+    }
+    static cudaError_t launch(const PassArgs &a, bool xin, bool xout, const SegTile *tiles,
+                              const uint32_t *counts, const uint32_t *hist, uint32_t grid,
+                              cudaStream_t s) {
+        if (xin) return xout ? one<true, true>(a, tiles, counts, hist, grid, s)
+                             : one<true, false>(a, tiles, counts, hist, grid, s);
+        return xout ? one<false, true>(a, tiles, counts, hist, grid, s)
+                    : one<false, false>(a, tiles, counts, hist, grid, s);
+    }
+};
+
+// ------------------------------------------------------------------- small
+// One warp per small segment (grid-stride over the list), padded to the next
+// power of two >= 32; the network is chosen per warp by the padded length.
+// Keys only: the network sorts the mapped keys (padding 0xFFFFFFFF ties with
+// real maximum keys, which is harmless: equal keys are identical).  With
+// values: it sorts (mapped key << 32 | position) composites (padding all
+// ones sorts after every real composite), and the values are gathered from a
+// shared-memory copy of the segment by the position.
+template <int LOG_R, bool PAIRS, bool XF>
+__device__ __forceinline__ void sort_small(const uint32_t *keys_in, uint32_t *keys_out,
+                                           const uint32_t *vals_in, uint32_t *vals_out,
+                                           uint32_t a, uint32_t len, uint32_t lane,
+                                           uint32_t fmask, uint32_t flip,
+                                           typename std::conditional<PAIRS, uint64_t, uint32_t>::type *sw,
+                                           uint32_t *sv) {
+    using E = typename std::conditional<PAIRS, uint64_t, uint32_t>::type;
+    constexpr int R = 1 << LOG_R;
+#pragma unroll
+    for (int c = 0; c < R; ++c) {
+        const uint32_t e = c * 32 + lane;
+        E x = ~E(0);
+        if (e < len) {
+            uint32_t k = keys_in[a + e];
+            if (XF) k = order_in<uint32_t>(k, fmask, flip);
+            if constexpr (PAIRS) {
+                x = (static_cast<uint64_t>(k) << 32) | e;
+                sv[e] = vals_in[a + e];
+            } else {
+                x = k;
+            }
+        }
+        sw[e + (e >> 5)] = x;
+    }
+    __syncwarp();
+    E x[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const uint32_t e = lane * R + r;
+        x[r] = sw[e + (e >> 5)];
+    }
+    bitonic_registers<LOG_R>(x, lane);
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const uint32_t e = lane * R + r;
+        sw[e + (e >> 5)] = x[r];
+    }
+    __syncwarp();
+#pragma unroll
+    for (int c = 0; c < R; ++c) {
+        const uint32_t e = c * 32 + lane;
+        if (e < len) {
+            const E y = sw[e + (e >> 5)];
+            uint32_t k;
+            if constexpr (PAIRS) {
+                k = static_cast<uint32_t>(y >> 32);
+                vals_out[a + e] = sv[static_cast<uint32_t>(y) & 0x3FFu];
+            } else {
+                k = y;
+            }
+            keys_out[a + e] = XF ? order_out<uint32_t>(k, fmask, flip) : k;
+        }
+    }
+    __syncwarp();   // the warp's staging buffers are free for its next segment
+}
+
+template <bool PAIRS, bool XF>
+__global__ void __launch_bounds__(kSmallWarps * 32)
+k_seg_small(const uint32_t *offsets, const uint32_t *small_list, const uint32_t *counts,
+            uint32_t small_max, const uint32_t *keys_in, uint32_t *keys_out, const uint32_t *vals_in,
+            uint32_t *vals_out, uint32_t fmask, uint32_t flip, const uint32_t *abort_flag) {
+    using E = typename std::conditional<PAIRS, uint64_t, uint32_t>::type;
+    constexpr uint32_t kPadded = kSmallMax + kSmallMax / 32;
+    extern __shared__ __align__(16) unsigned char s_raw[];
+    const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    E *sw = reinterpret_cast<E *>(s_raw) + warp * kPadded;
+    uint32_t *sv = reinterpret_cast<uint32_t *>(reinterpret_cast<E *>(s_raw) + kSmallWarps * kPadded) +
+                   warp * kSmallMax;
+    if (ld_relaxed(abort_flag)) return;
+    const uint32_t count = min(counts[0], small_max);
+    const uint32_t warps = gridDim.x * kSmallWarps;
+    for (uint32_t i = blockIdx.x * kSmallWarps + warp; i < count; i += warps) {
+        const uint32_t s = small_list[i];
+        const uint32_t a = offsets[s];
+        const uint32_t len = offsets[s + 1] - a;   // 2 .. 1024, checked by the classifier
+        const uint32_t log_lp = 32 - __clz(max(len, 32u) - 1);   // padded length 2^log_lp
+        switch (log_lp) {
+            case 5: sort_small<0, PAIRS, XF>(keys_in, keys_out, vals_in, vals_out, a, len, lane, fmask, flip, sw, sv); break;
+            case 6: sort_small<1, PAIRS, XF>(keys_in, keys_out, vals_in, vals_out, a, len, lane, fmask, flip, sw, sv); break;
+            case 7: sort_small<2, PAIRS, XF>(keys_in, keys_out, vals_in, vals_out, a, len, lane, fmask, flip, sw, sv); break;
+            case 8: sort_small<3, PAIRS, XF>(keys_in, keys_out, vals_in, vals_out, a, len, lane, fmask, flip, sw, sv); break;
+            case 9: sort_small<4, PAIRS, XF>(keys_in, keys_out, vals_in, vals_out, a, len, lane, fmask, flip, sw, sv); break;
+            default: sort_small<5, PAIRS, XF>(keys_in, keys_out, vals_in, vals_out, a, len, lane, fmask, flip, sw, sv); break;
+        }
+    }
+}
+
+template <bool PAIRS, bool XF>
+cudaError_t launch_small(const uint32_t *offsets, const uint32_t *small_list, const uint32_t *counts,
+                         uint32_t small_max, const uint32_t *keys_in, uint32_t *keys_out,
+                         const uint32_t *vals_in, uint32_t *vals_out, uint32_t fmask, uint32_t flip,
+                         const uint32_t *abort_flag, uint32_t grid, cudaStream_t s) {
+    using E = typename std::conditional<PAIRS, uint64_t, uint32_t>::type;
+    constexpr uint32_t kPadded = kSmallMax + kSmallMax / 32;
+    const size_t smem = kSmallWarps * (kPadded * sizeof(E) + (PAIRS ? kSmallMax * sizeof(uint32_t) : 0));
+    auto k = k_seg_small<PAIRS, XF>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    k<<<grid, kSmallWarps * 32, smem, s>>>(offsets, small_list, counts, small_max, keys_in, keys_out,
+                                           vals_in, vals_out, fmask, flip, abort_flag);
+    return cudaGetLastError();
+}
+
+void record(cudaEvent_t *ev, int num, int idx, cudaStream_t s) {
+    if (ev != nullptr && idx < num && ev[idx] != nullptr) cudaEventRecord(ev[idx], s);
+}
+
+}  // namespace
+
+SegLayout seg_layout(uint32_t n, uint32_t num_segments, bool with_values) {
+    SegLayout L{};
+    L.small_max = std::min<uint32_t>(num_segments, n / 2);
+    L.large_max = std::min<uint32_t>(num_segments, n / (kSmallMax + 1));
+    L.tiles_max = (n + kSegTile - 1) / kSegTile + L.large_max;
+    size_t off = kHdrBytes;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += align_up(std::max<size_t>(bytes, 1), kWsAlign);
+        return at;
+    };
+    L.small_list = take(static_cast<size_t>(L.small_max) * 4);
+    L.large_start = take(static_cast<size_t>(L.large_max) * 4);
+    L.large_len = take(static_cast<size_t>(L.large_max) * 4);
+    L.tile_base = take((static_cast<size_t>(L.large_max) + 1) * 4);
+    L.tiles = take(static_cast<size_t>(L.tiles_max) * sizeof(SegTile));
+    L.hist = take(static_cast<size_t>(L.large_max) * 1024 * 4);
+    L.look_a = take(static_cast<size_t>(L.tiles_max) * 256 * 4);
+    L.look_b = take(static_cast<size_t>(L.tiles_max) * 256 * 4);
+    L.tmp_keys = take(static_cast<size_t>(n) * 4);
+    L.tmp_vals = with_values ? take(static_cast<size_t>(n) * 4) : off;
+    L.total = off;
+    return L;
+}
+
+int launch_segmented_sort(const SegLaunch &L) {
+    const bool pairs = L.vals_in != nullptr;
+    const SegLayout lay = seg_layout(L.n, L.num_segments, pairs);
+    const KeyOrder order = key_order(L.kind, L.flags);
+    const bool mapped = order.fmask != 0 || order.flip != 0;
+    const uint32_t fmask = static_cast<uint32_t>(order.fmask), flip = static_cast<uint32_t>(order.flip);
+    cudaStream_t s = L.stream;
+    unsigned char *ws = L.ws;
+    uint32_t *status = reinterpret_cast<uint32_t *>(ws + kHdrStatus);
+    uint32_t *abort_flag = reinterpret_cast<uint32_t *>(ws + kHdrAbort);
+    uint32_t *counts = reinterpret_cast<uint32_t *>(ws + kHdrSegCounts);
+    uint32_t *small_list = reinterpret_cast<uint32_t *>(ws + lay.small_list);
+    uint32_t *large_start = reinterpret_cast<uint32_t *>(ws + lay.large_start);
+    uint32_t *large_len = reinterpret_cast<uint32_t *>(ws + lay.large_len);
+    uint32_t *tile_base = reinterpret_cast<uint32_t *>(ws + lay.tile_base);
+    SegTile *tiles = reinterpret_cast<SegTile *>(ws + lay.tiles);
+    uint32_t *hist = reinterpret_cast<uint32_t *>(ws + lay.hist);
+    uint32_t *look[2] = {reinterpret_cast<uint32_t *>(ws + lay.look_a),
+                         reinterpret_cast<uint32_t *>(ws + lay.look_b)};
+    uint32_t *tmp_k = reinterpret_cast<uint32_t *>(ws + lay.tmp_keys);
+    uint32_t *tmp_v = pairs ? reinterpret_cast<uint32_t *>(ws + lay.tmp_vals) : nullptr;
+    const uint32_t sms = static_cast<uint32_t>(L.sm_count);
+
+    record(L.events, L.num_events, 0, s);
+    k_zero_words<<<1, 256, 0, s>>>(reinterpret_cast<uint32_t *>(ws), static_cast<uint32_t>(kHdrBytes / 4));
+    if (cudaGetLastError() != cudaSuccess) return GSORT_ECUDA;
+    const uint32_t cgrid = std::max(1u, std::min((L.num_segments + 255) / 256, sms * 8));
+    k_seg_classify<<<cgrid, 256, 0, s>>>(L.offsets, L.num_segments, L.n, small_list, lay.small_max,
+                                         large_start, large_len, lay.large_max,
+                                         reinterpret_cast<uint4 *>(hist), L.keys_in, L.keys_out,
+                                         L.vals_in, L.vals_out, counts, status, abort_flag);
+    if (cudaGetLastError() != cudaSuccess) return GSORT_ECUDA;
+    record(L.events, L.num_events, 1, s);
+
+    // small segments first: independent of the large-segment kernels
+    const uint32_t sgrid = std::max(1u, std::min((lay.small_max + kSmallWarps - 1) / kSmallWarps, sms * 16));
+    cudaError_t e;
+    if (pairs)
+        e = mapped ? launch_small<true, true>(L.offsets, small_list, counts, lay.small_max, L.keys_in, L.keys_out,
+                                              L.vals_in, L.vals_out, fmask, flip, abort_flag, sgrid, s)
+                   : launch_small<true, false>(L.offsets, small_list, counts, lay.small_max, L.keys_in, L.keys_out,
+                                               L.vals_in, L.vals_out, fmask, flip, abort_flag, sgrid, s);
+    else
+        e = mapped ? launch_small<false, true>(L.offsets, small_list, counts, lay.small_max, L.keys_in, L.keys_out,
+                                               nullptr, nullptr, fmask, flip, abort_flag, sgrid, s)
+                   : launch_small<false, false>(L.offsets, small_list, counts, lay.small_max, L.keys_in, L.keys_out,
+                                                nullptr, nullptr, fmask, flip, abort_flag, sgrid, s);
+    if (e != cudaSuccess) return GSORT_ECUDA;
+    record(L.events, L.num_events, 2, s);
+    if (lay.large_max == 0) {
+        for (int i = 3; i < 8; ++i) record(L.events, L.num_events, i, s);
+        return GSORT_OK;
+    }
+
+    k_seg_scan<<<1, kScanThreads, 0, s>>>(large_len, lay.large_max, lay.tiles_max, tile_base, counts,
+                                          status, abort_flag);
+    if (cudaGetLastError() != cudaSuccess) return GSORT_ECUDA;
+    const uint32_t mgrid = std::max(1u, std::min((lay.large_max + 7) / 8, sms * 8));
+    k_seg_tilemap<<<mgrid, 256, 0, s>>>(large_start, large_len, tile_base, counts, lay.large_max, tiles,
+                                        abort_flag);
+    if (cudaGetLastError() != cudaSuccess) return GSORT_ECUDA;
+    const uint32_t hgrid = std::max(1u, std::min(lay.tiles_max, sms * 8));
+    if (mapped)
+        k_seg_hist<true><<<hgrid, 256, 0, s>>>(L.keys_in, tiles, counts, fmask, flip, hist, look[0], abort_flag);
+    else
+        k_seg_hist<false><<<hgrid, 256, 0, s>>>(L.keys_in, tiles, counts, fmask, flip, hist, look[0], abort_flag);
+    if (cudaGetLastError() != cudaSuccess) return GSORT_ECUDA;
+    record(L.events, L.num_events, 3, s);
+
+    // in -> tmp -> out -> tmp -> out (also when in == out: each pass reads
+    // what the previous one wrote)
+    const uint32_t pgrid = std::max(1u, std::min(lay.tiles_max, sms * 2));
+    const uint32_t *src_k = L.keys_in;
+    const uint32_t *src_v = L.vals_in;
+    for (int p = 0; p < 4; ++p) {
+        uint32_t *dst_k = (p % 2 == 0) ? tmp_k : L.keys_out;
+        uint32_t *dst_v = pairs ? ((p % 2 == 0) ? tmp_v : L.vals_out) : nullptr;
+        PassArgs a;
+        a.src_k = src_k;
+        a.dst_k = dst_k;
+        a.src_v = src_v;
+        a.dst_v = dst_v;
+        a.n = L.n;
+        a.shift = static_cast<uint32_t>(8 * p);
+        a.mask = 0xFFu;
+        a.fmask = order.fmask;
+        a.flip = order.flip;
+        a.hist = nullptr;   // per segment, from the tile descriptor
+        a.look = look[p & 1];
+        a.look_clear = (p + 1 < 4) ? look[(p + 1) & 1] : nullptr;
+        a.tile_counter = reinterpret_cast<uint32_t *>(ws + kHdrCounters + 128 * p);
+        a.status = status;
+        a.abort_flag = abort_flag;
+        a.spin_limit = L.spin_limit;
+        a.stall_tile = kNoStall;
+        const bool xin = mapped && p == 0, xout = mapped && p == 3;
+        e = pairs ? SegPassLaunch<true>::launch(a, xin, xout, tiles, counts, hist, pgrid, s)
+                  : SegPassLaunch<false>::launch(a, xin, xout, tiles, counts, hist, pgrid, s);
+        if (e != cudaSuccess) return GSORT_ECUDA;
+        record(L.events, L.num_events, 4 + p, s);
+        src_k = dst_k;
+        src_v = dst_v;
+    }
+    return GSORT_OK;
+}
+
+}  // namespace gsort

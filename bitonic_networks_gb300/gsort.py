@@ -194,6 +194,62 @@ def sort(keys: torch.Tensor, values: torch.Tensor | None = None, *, descending: 
     return ko, vo
 
 
+def segmented_sort_workspace_bytes(n: int, num_segments: int, with_values: bool) -> int:
+    return int(_lib.load().gsort_segmented_sort_workspace_bytes(n, num_segments,
+                                                                 1 if with_values else 0))
+
+
+def segmented_sort(keys: torch.Tensor, offsets: torch.Tensor, values: torch.Tensor | None = None,
+                   *, descending: bool = False, kind: int | None = None,
+                   keys_out: torch.Tensor | None = None, values_out: torch.Tensor | None = None,
+                   workspace: torch.Tensor | None = None, events=None, check: bool = True):
+    """Stable sort of each segment [offsets[s], offsets[s+1]) of 32-bit keys
+    (and 32-bit values).  offsets: int32/uint32 tensor of num_segments + 1
+    entries, 0 first and len(keys) last.  Returns (keys, values or None)."""
+    if not keys.is_cuda:
+        return _host_roundtrip(
+            lambda k, o, v: segmented_sort(k, o, v, descending=descending, kind=kind),
+            keys, offsets, values)
+    k = _flat_cuda(keys, "keys")
+    if kind is None:
+        if k.dtype not in _KIND_OF_DTYPE:
+            raise TypeError(f"no key kind for dtype {k.dtype}; pass kind=")
+        kind = _KIND_OF_DTYPE[k.dtype]
+    if _KIND_BYTES.get(kind) != 4 or k.element_size() != 4:
+        raise TypeError("segmented_sort takes 32-bit keys")
+    off = _flat_cuda(offsets, "offsets")
+    if off.element_size() != 4:
+        raise TypeError("offsets must be a 32-bit tensor")
+    v = None
+    if values is not None:
+        v = _flat_cuda(values, "values")
+        if v.numel() != k.numel() or v.element_size() != 4:
+            raise ValueError("values must be a 32-bit tensor with one entry per key")
+    n, S = k.numel(), max(off.numel() - 1, 0)
+    ko = torch.empty_like(k) if keys_out is None else _flat_cuda(keys_out, "keys_out")
+    vo = None
+    if v is not None:
+        vo = torch.empty_like(v) if values_out is None else _flat_cuda(values_out, "values_out")
+    lib = _lib.load()
+    ws = _workspace(segmented_sort_workspace_bytes(n, S, v is not None), k.device, workspace)
+    ev, nev = _events_arg(events)
+    opt = _lib.Options(0, -1, ctypes.cast(ev, ctypes.POINTER(ctypes.c_void_p))
+                       if ev is not None else None, nev, 0)
+    with torch.cuda.device(k.device):
+        rc = lib.gsort_segmented_sort_ex(
+            k.data_ptr(), ko.data_ptr(), v.data_ptr() if v is not None else None,
+            vo.data_ptr() if vo is not None else None, n, off.data_ptr(), S, kind,
+            DESCENDING if descending else 0, ws.data_ptr(), ws.numel(), _stream(k.device),
+            ctypes.byref(opt))
+        _check(rc, "gsort_segmented_sort")
+        if check and n > 0:
+            _check(lib.gsort_check(ws.data_ptr(), _stream(k.device)), "gsort_segmented_sort (device)")
+    ko = ko.view(keys.shape) if keys_out is None else keys_out
+    if vo is not None:
+        vo = vo.view(values.shape) if values_out is None else values_out
+    return ko, vo
+
+
 def sort_keys(keys: torch.Tensor, **kw) -> torch.Tensor:
     """Ascending sort of 32-bit keys (all 32 bits)."""
     if not keys.is_cuda:

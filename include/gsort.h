@@ -212,6 +212,40 @@ int gsort_segmented_bitonic(uint32_t *d_keys, int64_t num_segments,
                             int segment_len, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Variable-length segmented sort  ([PMPP10] 10.5, strategy 2: radix sort
+ * for the coarse order with bitonic networks for the small pieces;
+ * [GPUSORT]: pieces of <= 1024 keys go to a bitonic sort)
+ *
+ * d_offsets holds num_segments + 1 uint32 entries with d_offsets[0] == 0,
+ * d_offsets[s] <= d_offsets[s + 1] and d_offsets[num_segments] == n; segment
+ * s is keys [d_offsets[s], d_offsets[s + 1]).  Each segment is sorted
+ * stably by the whole key of `kind` (32-bit kinds: GSORT_KEY_U32, F32, I32;
+ * others: GSORT_EINVAL), ascending, or descending with GSORT_DESCENDING;
+ * equal keys keep their input order and values (optional, 32-bit) move
+ * with their keys.  Segments of 2..1024 keys are sorted by one warp each
+ * (register bitonic network; with values it sorts (key, position) pairs,
+ * which makes it stable); longer segments by a radix sort whose tiles never
+ * cross a segment boundary.  Empty segments are allowed.
+ *
+ * Offsets are read on the device: offsets that break the rules above make
+ * the call record GSORT_EINVAL in the workspace (returned by gsort_check)
+ * and leave the output unspecified; no memory outside the given arrays is
+ * touched.  n == 0 is a no-op (the offsets are not read); num_segments == 0
+ * requires n == 0.  In place (in == out, for keys and for values) is
+ * allowed; other overlaps: GSORT_EINVAL.  The workspace comes from
+ * gsort_segmented_sort_workspace_bytes(): 4.25 bytes per key for keys
+ * only (8.25 with values) when every segment is long, growing with the
+ * number of segments up to about 12.3 (16.3) bytes per key.
+ * ---------------------------------------------------------------------- */
+size_t gsort_segmented_sort_workspace_bytes(int64_t n, int64_t num_segments, int with_values);
+
+int gsort_segmented_sort(const void *d_keys_in, void *d_keys_out,
+                         const uint32_t *d_vals_in, uint32_t *d_vals_out, int64_t n,
+                         const uint32_t *d_offsets, int64_t num_segments,
+                         int kind, int flags, void *d_ws, size_t ws_bytes,
+                         cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Device-side status: synchronises `stream`, then returns GSORT_OK or the
  * error a kernel recorded in this workspace during the last call that used
  * it (GSORT_ETIMEOUT), or GSORT_ECUDA if the stream reports an error.
@@ -253,6 +287,15 @@ int gsort_radix_sort_ex(const void *d_keys_in, void *d_keys_out,
                         int kind, int flags, int begin_bit, int end_bit,
                         void *d_ws, size_t ws_bytes, cudaStream_t stream,
                         const gsort_options *options);
+
+/* Events for the segmented sort: [0] start, [1] after the classification,
+ * [2] after the small segments, [3] after the large segments' histograms,
+ * [4 + p] after digit pass p of the large segments. */
+int gsort_segmented_sort_ex(const void *d_keys_in, void *d_keys_out,
+                            const uint32_t *d_vals_in, uint32_t *d_vals_out, int64_t n,
+                            const uint32_t *d_offsets, int64_t num_segments,
+                            int kind, int flags, void *d_ws, size_t ws_bytes,
+                            cudaStream_t stream, const gsort_options *options);
 
 int gsort_compact_positive_ex(const float *d_in, float *d_out, int64_t n,
                               int64_t *d_num_kept, void *d_ws, size_t ws_bytes,

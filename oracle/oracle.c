@@ -367,6 +367,41 @@ int oracle_radix_sort_general(const void *keys_in, const uint32_t *vals_in,
 }
 
 /* ---------------------------------------------------------------------------
+ * NEXT (f2): variable-length segments.  Segment s is [offsets[s],
+ * offsets[s+1]); the offsets must start at 0, never decrease and end at n.
+ * Each segment is sorted on its own by the stable sort above (every 32-bit
+ * kind, either direction), which is the definition of a stable segmented
+ * sort ([PMPP10] 10.5 names the hybrid strategy; the result it must reach is
+ * each piece sorted).  Returns ORACLE_EINVAL for offsets that break the rules.
+ * ------------------------------------------------------------------------- */
+int oracle_segmented_sort_general(const uint32_t *keys_in, const uint32_t *vals_in,
+                                  uint32_t *keys_out, uint32_t *vals_out, int64_t n,
+                                  const uint32_t *offsets, int64_t num_segments,
+                                  int kind, int flags)
+{
+    if (oracle_kind_bytes(kind) != 4 || n < 0 || num_segments < 0)
+        return ORACLE_EINVAL;
+    if (n == 0)
+        return ORACLE_OK;
+    if (num_segments == 0 || offsets[0] != 0 || offsets[num_segments] != (uint32_t)n)
+        return ORACLE_EINVAL;
+    for (int64_t s = 0; s < num_segments; ++s)
+        if (offsets[s + 1] < offsets[s])
+            return ORACLE_EINVAL;
+    int with_vals = (vals_in != NULL && vals_out != NULL);
+    for (int64_t s = 0; s < num_segments; ++s) {
+        uint32_t a = offsets[s];
+        int64_t len = (int64_t)offsets[s + 1] - a;
+        int rc = oracle_radix_sort_general(keys_in + a, with_vals ? vals_in + a : NULL,
+                                           keys_out + a, with_vals ? vals_out + a : NULL,
+                                           len, kind, flags, 0, 32);
+        if (rc != ORACLE_OK)
+            return rc;
+    }
+    return ORACLE_OK;
+}
+
+/* ---------------------------------------------------------------------------
  * a4: stream compaction, the 1-bit special case ([CUDA3] "Stream
  * Compaction": predicate, exclusive scan of the predicate, scatter).  Keeps
  * every x > 0 in input order at out[0..m), writes +0.0 to out[m..n), and

@@ -106,6 +106,8 @@ class Oracle:
                                                    _u32p]),
         "oracle_radix_sort_general": (_int, [ctypes.c_void_p, _u32p, ctypes.c_void_p, _u32p, _i64,
                                              _int, _int, _int, _int]),
+        "oracle_segmented_sort_general": (_int, [_u32p, _u32p, _u32p, _u32p, _i64, _u32p, _i64,
+                                                 _int, _int]),
     }
 
     def __init__(self, path: str):
@@ -214,6 +216,22 @@ class Oracle:
         _check(self.lib.oracle_radix_sort_general(k.ctypes.data, _ptr(v), ko.ctypes.data, _ptr(vo),
                                                   k.size, kind, int(descending), begin_bit,
                                                   end_bit), "radix_sort_general")
+        return ko, vo
+
+    # f2: variable-length segments --------------------------------------
+    def segmented_sort_general(self, keys, offsets, vals=None, kind: int = 0,
+                               descending: bool = False):
+        """(keys_out with the input dtype, vals_out or None); raises on bad offsets."""
+        k = _as_kind(keys, kind)
+        off = np.ascontiguousarray(offsets, dtype=np.uint32).ravel()
+        ko = np.empty_like(k)
+        v = vo = None
+        if vals is not None:
+            v = _as_u32(vals).ravel()
+            vo = np.empty_like(v)
+        _check(self.lib.oracle_segmented_sort_general(
+            _ptr(k.view(np.uint32)), _ptr(v), _ptr(ko.view(np.uint32)), _ptr(vo), k.size, _ptr(off),
+            max(off.size - 1, 0), kind, int(descending)), "segmented_sort_general")
         return ko, vo
 
     # a4 -----------------------------------------------------------------

@@ -119,6 +119,29 @@ def test_general_argument_errors(lib):
     assert h(A, 10, 6, 0, 8, B, None) == EINVAL
 
 
+def test_segmented_sort_argument_errors(lib):
+    big = 1 << 40
+    O = 0x30000000
+    f = lib.gsort_segmented_sort
+    assert f(A, B, None, None, 0, O, 5, 0, 0, None, 0, None) == 0              # n == 0: no-op
+    assert f(A, B, None, None, 10, O, 0, 0, 0, W, big, None) == EINVAL         # keys but no segment
+    assert f(A, B, None, None, -1, O, 1, 0, 0, W, big, None) == EINVAL
+    assert f(A, B, None, None, 1 << 30, O, 1, 0, 0, W, big, None) == ETOOBIG
+    assert f(A, B, None, None, 10, O, 1, 3, 0, W, big, None) == EINVAL         # 64-bit kind
+    assert f(A, B, None, None, 10, O, 1, 0, 4, W, big, None) == EINVAL         # unknown flag
+    assert f(A, B, None, None, 10, None, 1, 0, 0, W, big, None) == EINVAL
+    assert f(A, B, None, None, 10, O + 2, 1, 0, 0, W, big, None) == EALIGN
+    assert f(A, B, A + 0x1000, None, 10, O, 1, 0, 0, W, big, None) == EINVAL   # values half given
+    assert f(A, A + 4, None, None, 10, O, 1, 0, 0, W, big, None) == EINVAL     # partial overlap
+    assert f(A, B, None, None, 10, B + 8, 1, 0, 0, W, big, None) == EINVAL     # offsets inside the output
+    assert f(A, B, None, None, 10, O, 1, 0, 0, W, 64, None) == EWS
+    assert f(A, B, None, None, 10, O, 1, 0, 0, W + 8, big, None) == EALIGN
+    assert f(A, B, None, None, 10, O, 1, 0, 0, O, big, None) == EINVAL         # workspace over the offsets
+    ws = lib.gsort_segmented_sort_workspace_bytes
+    assert ws(-1, 1, 0) == 0 and ws(10, -1, 0) == 0 and ws(1 << 30, 1, 0) == 0
+    assert ws(1 << 20, 1, 1) > ws(1 << 20, 1, 0) > 4 * (1 << 20)
+
+
 def test_launch_count(lib):
     assert lib.gsort_radix_launch_count(100, 0, 32, 0) == 6
     assert lib.gsort_radix_launch_count(100, 0, 8, 0) == 3

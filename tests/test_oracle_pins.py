@@ -541,6 +541,51 @@ def test_general_matches_32bit_oracle(orc):
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
+# ------------------------------------------------ f2: variable-length segments
+
+def _segment_lengths(rng, n_target):
+    lens = []
+    total = 0
+    while total < n_target:
+        r = rng.random()
+        L = int(rng.integers(0, 3)) if r < 0.3 else int(rng.integers(3, 40)) if r < 0.8 \
+            else int(rng.integers(40, 3000))
+        lens.append(L)
+        total += L
+    return np.array(lens, dtype=np.int64)
+
+
+def pin_segmented_general(orc):
+    rng = np.random.default_rng(31)
+    for kind in (0, 1, 2):
+        for desc in (False, True):
+            lens = _segment_lengths(rng, 6000)
+            off = np.concatenate([[0], np.cumsum(lens)]).astype(np.uint32)
+            n = int(off[-1])
+            keys = _edge_keys(kind, n, 400 + kind) if n else np.zeros(0, KIND_DTYPE[kind])
+            idx = np.arange(n, dtype=np.uint32)
+            ko, vo = orc.segmented_sort_general(keys, off, idx, kind, desc)
+            key = _py_key(kind)
+            for s in range(lens.size):
+                a, b = int(off[s]), int(off[s + 1])
+                exp = sorted(range(a, b), key=lambda i: key(keys[i]), reverse=desc)
+                assert vo[a:b].tolist() == exp, (kind, desc, s)
+            assert np.array_equal(ko.view(np.uint8), keys[vo].view(np.uint8))
+
+
+def test_segmented_general(orc):
+    pin_segmented_general(orc)
+
+
+def test_segmented_general_rejects_bad_offsets(orc):
+    keys = np.arange(10, dtype=np.uint32)[::-1].copy()
+    for off in ([1, 10], [0, 9], [0, 6, 4, 10], [0, 11]):
+        with pytest.raises(RuntimeError):
+            orc.segmented_sort_general(keys, np.array(off), None, 0)
+    ko, _ = orc.segmented_sort_general(keys, np.array([0, 0, 10, 10]), None, 0)
+    assert ko.tolist() == list(range(10))
+
+
 MUTANTS = {
     # a reversed scatter: each pass is no longer stable
     "unstable_scatter": ("for (int64_t i = 0; i < n; ++i) {\n            uint32_t d = digit_of",
@@ -571,6 +616,9 @@ MUTANTS = {
     "f64_sign_only": ("        if (bits >> 63)\n            u = ~bits;",
                       "        if (bits >> 63)\n            u = bits ^ 0x8000000000000000ull;"),
     # f1: descending complement at 32 bits for every width
+    # f2: the last segment is left unsorted
+    "segmented_last": ("for (int64_t s = 0; s < num_segments; ++s) {\n        uint32_t a = offsets[s];",
+                       "for (int64_t s = 0; s + 1 < num_segments; ++s) {\n        uint32_t a = offsets[s];"),
     "descending_width": ("    }\n    if (descending)\n        u = (w == 64 ? 0xFFFFFFFFFFFFFFFFull : 0xFFFFFFFFull) - u;",
                          "    }\n    if (descending)\n        u = 0xFFFFFFFFull - u;"),
 }
@@ -579,7 +627,8 @@ PINS = [pin_radix_worked_example, pin_compaction_worked_example, pin_bitonic_exe
         pin_transform_matches_float_compare, pin_histograms_constructed,
         pin_sort_vs_python_sorted, pin_float_sort_vs_python_sorted,
         pin_compaction_specials, pin_bitonic_zero_one, pin_segmented_vs_numpy,
-        pin_general_vs_python_sorted, pin_general_bit_range, pin_general_maps]
+        pin_general_vs_python_sorted, pin_general_bit_range, pin_general_maps,
+        pin_segmented_general]
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
