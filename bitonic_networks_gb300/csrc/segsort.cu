@@ -257,7 +257,7 @@ struct SegPassLaunch {
 
 // ------------------------------------------------------------------- small
 // One warp per small segment (grid-stride over the list), padded to the next
-// power of two >= 32; the network is chosen per warp by the padded length.
+// power of two >= 32.
 // Keys only: the network sorts the mapped keys (padding 0xFFFFFFFF ties with
 // real maximum keys, which is harmless: equal keys are identical).  With
 // values: it sorts (mapped key << 32 | position) composites (padding all
@@ -321,18 +321,22 @@ __device__ __forceinline__ void sort_small(const uint32_t *keys_in, uint32_t *ke
     __syncwarp();   // the warp's staging buffers are free for its next segment
 }
 
-template <bool PAIRS, bool XF>
+// One kernel per padded length 2^(5+LOG_R): every kernel walks the whole list
+// and takes the segments of its length class, so that each network gets the
+// registers it needs (one kernel holding all six would be sized by the largest).
+template <int LOG_R, bool PAIRS, bool XF>
 __global__ void __launch_bounds__(kSmallWarps * 32)
 k_seg_small(const uint32_t *offsets, const uint32_t *small_list, const uint32_t *counts,
             uint32_t small_max, const uint32_t *keys_in, uint32_t *keys_out, const uint32_t *vals_in,
             uint32_t *vals_out, uint32_t fmask, uint32_t flip, const uint32_t *abort_flag) {
     using E = typename std::conditional<PAIRS, uint64_t, uint32_t>::type;
-    constexpr uint32_t kPadded = kSmallMax + kSmallMax / 32;
+    constexpr uint32_t kLp = 32u << LOG_R;
+    constexpr uint32_t kPadded = kLp + kLp / 32;
     extern __shared__ __align__(16) unsigned char s_raw[];
     const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     E *sw = reinterpret_cast<E *>(s_raw) + warp * kPadded;
     uint32_t *sv = reinterpret_cast<uint32_t *>(reinterpret_cast<E *>(s_raw) + kSmallWarps * kPadded) +
-                   warp * kSmallMax;
+                   warp * kLp;
     if (ld_relaxed(abort_flag)) return;
     const uint32_t count = min(counts[0], small_max);
     const uint32_t warps = gridDim.x * kSmallWarps;
@@ -341,15 +345,29 @@ k_seg_small(const uint32_t *offsets, const uint32_t *small_list, const uint32_t 
         const uint32_t a = offsets[s];
         const uint32_t len = offsets[s + 1] - a;   // 2 .. 1024, checked by the classifier
         const uint32_t log_lp = 32 - __clz(max(len, 32u) - 1);   // padded length 2^log_lp
-        switch (log_lp) {
-            case 5: sort_small<0, PAIRS, XF>(keys_in, keys_out, vals_in, vals_out, a, len, lane, fmask, flip, sw, sv); break;
-            case 6: sort_small<1, PAIRS, XF>(keys_in, keys_out, vals_in, vals_out, a, len, lane, fmask, flip, sw, sv); break;
-            case 7: sort_small<2, PAIRS, XF>(keys_in, keys_out, vals_in, vals_out, a, len, lane, fmask, flip, sw, sv); break;
-            case 8: sort_small<3, PAIRS, XF>(keys_in, keys_out, vals_in, vals_out, a, len, lane, fmask, flip, sw, sv); break;
-            case 9: sort_small<4, PAIRS, XF>(keys_in, keys_out, vals_in, vals_out, a, len, lane, fmask, flip, sw, sv); break;
-            default: sort_small<5, PAIRS, XF>(keys_in, keys_out, vals_in, vals_out, a, len, lane, fmask, flip, sw, sv); break;
-        }
+        if (log_lp != 5 + LOG_R) continue;          // warp-uniform
+        sort_small<LOG_R, PAIRS, XF>(keys_in, keys_out, vals_in, vals_out, a, len, lane, fmask, flip,
+                                     sw, sv);
     }
+}
+
+template <int LOG_R, bool PAIRS, bool XF>
+cudaError_t launch_small_class(const uint32_t *offsets, const uint32_t *small_list,
+                               const uint32_t *counts, uint32_t small_max, const uint32_t *keys_in,
+                               uint32_t *keys_out, const uint32_t *vals_in, uint32_t *vals_out,
+                               uint32_t fmask, uint32_t flip, const uint32_t *abort_flag,
+                               uint32_t grid, cudaStream_t s) {
+    using E = typename std::conditional<PAIRS, uint64_t, uint32_t>::type;
+    constexpr uint32_t kLp = 32u << LOG_R;
+    constexpr uint32_t kPadded = kLp + kLp / 32;
+    const size_t smem = kSmallWarps * (kPadded * sizeof(E) + (PAIRS ? kLp * sizeof(uint32_t) : 0));
+    auto k = k_seg_small<LOG_R, PAIRS, XF>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    k<<<grid, kSmallWarps * 32, smem, s>>>(offsets, small_list, counts, small_max, keys_in, keys_out,
+                                           vals_in, vals_out, fmask, flip, abort_flag);
+    return cudaGetLastError();
 }
 
 template <bool PAIRS, bool XF>
@@ -357,16 +375,20 @@ cudaError_t launch_small(const uint32_t *offsets, const uint32_t *small_list, co
                          uint32_t small_max, const uint32_t *keys_in, uint32_t *keys_out,
                          const uint32_t *vals_in, uint32_t *vals_out, uint32_t fmask, uint32_t flip,
                          const uint32_t *abort_flag, uint32_t grid, cudaStream_t s) {
-    using E = typename std::conditional<PAIRS, uint64_t, uint32_t>::type;
-    constexpr uint32_t kPadded = kSmallMax + kSmallMax / 32;
-    const size_t smem = kSmallWarps * (kPadded * sizeof(E) + (PAIRS ? kSmallMax * sizeof(uint32_t) : 0));
-    auto k = k_seg_small<PAIRS, XF>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    k<<<grid, kSmallWarps * 32, smem, s>>>(offsets, small_list, counts, small_max, keys_in, keys_out,
-                                           vals_in, vals_out, fmask, flip, abort_flag);
-    return cudaGetLastError();
+    cudaError_t e = cudaSuccess;
+#define GSORT_SMALL_CLASS(R)                                                                       \
+    if (e == cudaSuccess)                                                                          \
+        e = launch_small_class<R, PAIRS, XF>(offsets, small_list, counts, small_max, keys_in,      \
+                                             keys_out, vals_in, vals_out, fmask, flip, abort_flag, \
+                                             grid, s);
+    GSORT_SMALL_CLASS(0)
+    GSORT_SMALL_CLASS(1)
+    GSORT_SMALL_CLASS(2)
+    GSORT_SMALL_CLASS(3)
+    GSORT_SMALL_CLASS(4)
+    GSORT_SMALL_CLASS(5)
+#undef GSORT_SMALL_CLASS
+    return e;
 }
 
 void record(cudaEvent_t *ev, int num, int idx, cudaStream_t s) {

@@ -6,7 +6,8 @@
 OP: keys (uint32 keys, 32 bits), pairs (uint32 key/index pairs), fpairs
 (float keys with index values), compact (compaction input), segments (1024-key
 segments, n/1024 of them), hist (the digit-histogram step alone), sort (any
-key kind: --kind u32|f32|i32|u64|f64|i64 [--desc] [--values]).
+key kind: --kind u32|f32|i32|u64|f64|i64 [--desc] [--values]), segsort
+(variable-length segments, --mix small|mixed|large [--values] [--desc]).
 --time prints the median CUDA-event time of the timed calls.
 Each call is followed by a device-status check; the process exits non-zero on
 any error, so a profiler only ever runs a command that finished cleanly.
@@ -24,7 +25,9 @@ from . import _lib, gsort, synth
 
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=["keys", "pairs", "fpairs", "compact", "segments", "hist", "sort"])
+    ap.add_argument("op", choices=["keys", "pairs", "fpairs", "compact", "segments", "hist", "sort",
+                                   "segsort"])
+    ap.add_argument("--mix", choices=["small", "mixed", "large"], default="mixed")
     ap.add_argument("--kind", choices=["u32", "f32", "i32", "u64", "f64", "i64"], default="u64")
     ap.add_argument("--desc", action="store_true")
     ap.add_argument("--values", action="store_true")
@@ -43,7 +46,15 @@ def main(argv=None) -> int:
 
     kinds = {"u32": 0, "f32": 1, "i32": 2, "u64": 3, "f64": 4, "i64": 5}
     kind = kinds[a.kind]
-    if a.op == "sort":
+    if a.op == "segsort":
+        x = up(synth.uniform_keys(n, 7))
+        off_np = synth.segment_offsets(n, a.mix, 8)
+        off = up(off_np)
+        v = up(synth.index_values(n)) if a.values else None
+        print(f"segsort {a.mix}: {off_np.size - 1} segments, "
+              f"{int(((off_np[1:] - off_np[:-1]) <= 1024).sum())} of at most 1024 keys "
+              f"holding {int((off_np[1:] - off_np[:-1])[(off_np[1:] - off_np[:-1]) <= 1024].sum())} keys")
+    elif a.op == "sort":
         kx = synth.keys_of_kind(kind, n, 6)
         kx = kx.view({4: np.int32, 8: np.int64}[kx.dtype.itemsize]) if kx.dtype.kind == "u" else kx
         x = torch.from_numpy(np.ascontiguousarray(kx)).to(dev)
@@ -61,7 +72,9 @@ def main(argv=None) -> int:
         x = seg.clone()
 
     def once():
-        if a.op == "sort":
+        if a.op == "segsort":
+            gsort.segmented_sort(x, off, v, descending=a.desc, kind=0, check=not a.time)
+        elif a.op == "sort":
             gsort.sort(x, v, descending=a.desc, kind=kind, check=not a.time)
         elif a.op == "keys":
             gsort.sort_pairs(x, None, variant=a.variant)

@@ -169,6 +169,29 @@ def keys_of_kind(kind: int, n: int, seed: int = SEED_BASE) -> np.ndarray:
     return k
 
 
+def segment_offsets(n: int, mix: str, seed: int = SEED_BASE) -> np.ndarray:
+    """uint32 offsets (0 first, n last) of segments covering n keys:
+    "small": lengths uniform in [1, 1024]; "large": uniform in [8192, 2^20];
+    "mixed": log-uniform in [1, 2^17] (most segments short, most keys in
+    long segments).  The last segment takes what is left."""
+    rng_words = splitmix64(stream_seed(seed, 5), max(16, 4 * n // 512 + 64))
+    u = (rng_words >> np.uint64(11)).astype(np.float64) / float(1 << 53)
+    if mix == "small":
+        lens = 1 + np.floor(u * 1024).astype(np.int64)
+    elif mix == "large":
+        lens = 8192 + np.floor(u * (2**20 - 8192)).astype(np.int64)
+    elif mix == "mixed":
+        lens = np.floor(np.exp2(u * 17)).astype(np.int64)
+    else:
+        raise ValueError(mix)
+    ends = np.cumsum(lens)
+    k = int(np.searchsorted(ends, n))
+    if k >= lens.size:
+        raise ValueError("not enough segment lengths drawn")
+    off = np.concatenate([[0], ends[:k], [n]]).astype(np.uint32)
+    return off
+
+
 def compaction_input(n: int, seed: int = SEED_BASE) -> np.ndarray:
     """float32 drawn from {-U(0,1), 0.0, +U(0,1)} with probabilities
     0.4 / 0.2 / 0.4 (category from one stream, magnitude from another)."""
