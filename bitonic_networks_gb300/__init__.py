@@ -9,6 +9,7 @@ import importlib
 
 __all__ = [
     "sort", "sort_keys", "sort_pairs", "compact_positive", "segmented_sort_", "segmented_sort",
+    "partition", "split_sort",
     "digit_histograms", "GsortError", "library_path",
     "radix_workspace_bytes", "sort_workspace_bytes", "segmented_sort_workspace_bytes",
     "compact_workspace_bytes",

@@ -86,6 +86,15 @@ SIGNATURES = {
                                                ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
                                                ctypes.POINTER(Options)]),
+    "gsort_partition_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64]),
+    "gsort_partition": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                       ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_uint32, ctypes.c_void_p, ctypes.c_void_p,
+                                       ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "gsort_split_sort_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int]),
+    "gsort_split_sort": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
     "gsort_check": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "gsort_radix_num_variants": (ctypes.c_int, []),
     "gsort_radix_variant_name": (ctypes.c_char_p, [ctypes.c_int]),

@@ -349,6 +349,118 @@ int gsort_segmented_sort(const void *d_keys_in, void *d_keys_out, const uint32_t
                                    num_segments, kind, flags, d_ws, ws_bytes, stream, nullptr);
 }
 
+size_t gsort_partition_workspace_bytes(int64_t n) {
+    if (n < 0 || n > GSORT_MAX_N) return 0;
+    return split_layout(static_cast<uint32_t>(n), false, false).total;
+}
+
+int gsort_partition(const uint32_t *d_in, uint32_t *d_out, const uint32_t *d_vals_in,
+                    uint32_t *d_vals_out, int64_t n, int pred, int kind, uint32_t param,
+                    const uint8_t *d_flags, int64_t *d_num_true, void *d_ws, size_t ws_bytes,
+                    cudaStream_t stream) {
+    if (n < 0) return GSORT_EINVAL;
+    if (n > GSORT_MAX_N) return GSORT_ETOOBIG;
+    if (pred < GSORT_PRED_FLAGS || pred > GSORT_PRED_POSITIVE) return GSORT_EINVAL;
+    if ((pred == GSORT_PRED_BIT_SET || pred == GSORT_PRED_BIT_CLEAR) && param >= 32) return GSORT_EINVAL;
+    if (pred == GSORT_PRED_LESS && key_kind_bytes(kind) != 4) return GSORT_EINVAL;
+    if ((d_vals_in == nullptr) != (d_vals_out == nullptr)) return GSORT_EINVAL;
+    if (d_num_true != nullptr && !aligned(d_num_true, 8)) return GSORT_EALIGN;
+    const bool pairs = d_vals_in != nullptr;
+    if (n > 0) {
+        if (d_in == nullptr || d_out == nullptr) return GSORT_EINVAL;
+        if (pred == GSORT_PRED_FLAGS && d_flags == nullptr) return GSORT_EINVAL;
+        if (!aligned(d_in, 4) || !aligned(d_out, 4)) return GSORT_EALIGN;
+        if (pairs && (!aligned(d_vals_in, 4) || !aligned(d_vals_out, 4))) return GSORT_EALIGN;
+        const size_t bytes = static_cast<size_t>(n) * 4;
+        if (overlap(d_in, d_out, bytes)) return GSORT_EINVAL;
+        if (pairs && (overlap(d_vals_in, d_vals_out, bytes) || overlap(d_in, d_vals_out, bytes) ||
+                      overlap(d_vals_in, d_out, bytes) || overlap(d_out, d_vals_out, bytes)))
+            return GSORT_EINVAL;
+        if (pred == GSORT_PRED_FLAGS &&
+            (ranges_overlap(d_flags, static_cast<size_t>(n), d_out, bytes) ||
+             (pairs && ranges_overlap(d_flags, static_cast<size_t>(n), d_vals_out, bytes))))
+            return GSORT_EINVAL;
+    }
+    if (d_ws == nullptr) return GSORT_EWORKSPACE;
+    if (!aligned(d_ws, kWsAlign)) return GSORT_EALIGN;
+    const SplitLayout lay = split_layout(static_cast<uint32_t>(n), pairs, false);
+    if (ws_bytes < lay.total) return GSORT_EWORKSPACE;
+    if (n == 0) {
+        if (d_num_true != nullptr && cudaMemsetAsync(d_num_true, 0, sizeof(int64_t), stream) != cudaSuccess)
+            return GSORT_ECUDA;
+        return GSORT_OK;
+    }
+    const size_t bytes = static_cast<size_t>(n) * 4;
+    if (ranges_overlap(d_ws, ws_bytes, d_in, bytes) || ranges_overlap(d_ws, ws_bytes, d_out, bytes) ||
+        (pairs && (ranges_overlap(d_ws, ws_bytes, d_vals_in, bytes) ||
+                   ranges_overlap(d_ws, ws_bytes, d_vals_out, bytes))))
+        return GSORT_EINVAL;
+    DeviceInfo dev;
+    if (device_info(&dev) != GSORT_OK) return GSORT_ECUDA;
+    PartitionLaunch L;
+    L.in = d_in;
+    L.out = d_out;
+    L.vals_in = d_vals_in;
+    L.vals_out = d_vals_out;
+    L.n = static_cast<uint32_t>(n);
+    L.pred = pred;
+    L.kind = kind;
+    L.param = param;
+    L.flags = d_flags;
+    L.num_true = d_num_true;
+    L.ws = static_cast<unsigned char *>(d_ws);
+    L.spin_limit = kDefaultSpinLimit;
+    L.stream = stream;
+    L.sm_count = dev.sm_count;
+    return launch_partition(L);
+}
+
+size_t gsort_split_sort_workspace_bytes(int64_t n, int with_values) {
+    if (n < 0 || n > GSORT_MAX_N) return 0;
+    return split_layout(static_cast<uint32_t>(n), with_values != 0, true).total;
+}
+
+int gsort_split_sort(const uint32_t *d_keys_in, uint32_t *d_keys_out, const uint32_t *d_vals_in,
+                     uint32_t *d_vals_out, int64_t n, int begin_bit, int end_bit, void *d_ws,
+                     size_t ws_bytes, cudaStream_t stream) {
+    int rc = radix_args(d_keys_in, d_keys_out, d_vals_in, d_vals_out, n, GSORT_KEY_U32, 0, begin_bit,
+                        end_bit, &kDefaults);
+    if (rc != GSORT_OK || n == 0) return rc;
+    const bool pairs = d_vals_in != nullptr;
+    if (d_ws == nullptr) return GSORT_EWORKSPACE;
+    if (!aligned(d_ws, kWsAlign)) return GSORT_EALIGN;
+    if (ws_bytes < split_layout(static_cast<uint32_t>(n), pairs, true).total) return GSORT_EWORKSPACE;
+    const size_t bytes = static_cast<size_t>(n) * 4;
+    if (ranges_overlap(d_ws, ws_bytes, d_keys_in, bytes) || ranges_overlap(d_ws, ws_bytes, d_keys_out, bytes) ||
+        (pairs && (ranges_overlap(d_ws, ws_bytes, d_vals_in, bytes) ||
+                   ranges_overlap(d_ws, ws_bytes, d_vals_out, bytes))))
+        return GSORT_EINVAL;
+    if (begin_bit == end_bit) {
+        if (d_keys_out != d_keys_in &&
+            cudaMemcpyAsync(d_keys_out, d_keys_in, bytes, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+            return GSORT_ECUDA;
+        if (pairs && d_vals_out != d_vals_in &&
+            cudaMemcpyAsync(d_vals_out, d_vals_in, bytes, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+            return GSORT_ECUDA;
+        return GSORT_OK;
+    }
+    DeviceInfo dev;
+    if (device_info(&dev) != GSORT_OK) return GSORT_ECUDA;
+    SplitSortLaunch L;
+    L.keys_in = d_keys_in;
+    L.keys_out = d_keys_out;
+    L.vals_in = d_vals_in;
+    L.vals_out = d_vals_out;
+    L.n = static_cast<uint32_t>(n);
+    L.begin_bit = begin_bit;
+    L.end_bit = end_bit;
+    L.ws = static_cast<unsigned char *>(d_ws);
+    L.spin_limit = kDefaultSpinLimit;
+    L.stream = stream;
+    L.sm_count = dev.sm_count;
+    return launch_split_sort(L);
+}
+
 int gsort_radix_num_variants(void) { return radix_num_variants(); }
 
 const char *gsort_radix_variant_name(int variant) { return radix_variant_name(variant); }

@@ -12,7 +12,7 @@
 #include <algorithm>
 #include <mutex>
 
-#include "gsort_internal.cuh"
+#include "lookback.cuh"
 
 namespace gsort {
 namespace {
@@ -20,7 +20,6 @@ namespace {
 constexpr int kCompactThreads = 512;
 constexpr int kCompactItems = 16;          // per thread, a multiple of 4
 constexpr uint32_t kCompactTile = kCompactThreads * kCompactItems;
-constexpr int kCompactLookChunks = 1;      // look-back window: 32 predecessor tiles per round
 // One look-back word per 128-byte line: hundreds of waiting tiles poll their
 // predecessors' words at once, and packing the words densely puts all of that
 // polling on a few L2 lines.  Spread out, the polls of one window hit 32 lines.
@@ -98,54 +97,10 @@ k_compact(const uint32_t *__restrict__ in, uint32_t *__restrict__ out, uint32_t 
     uint32_t pos = warp_excl + incl - cnt;
 
     if (warp == 0) {
-        // publish the tile count at once, then look back: lane l inspects tile (t - 1 - l)
-        uint32_t prefix = 0;
-        bool ok = true;
-        if (lane == 0 && tile != stall_tile)
-            st_relaxed(states + tile * kStateStride, (tile == 0 ? kFlagPrefix : kFlagAgg) | total);
-        if (tile > 0 && tile != stall_tile) {
-            // a round reads 4 x 32 predecessors: lane l of chunk q inspects tile t - 32q - l
-            int32_t t = static_cast<int32_t>(tile) - 1 - static_cast<int32_t>(lane);
-            uint32_t polls = 0, ns = 32;
-            while (true) {
-                uint32_t s[kCompactLookChunks];
-#pragma unroll
-                for (int q = 0; q < kCompactLookChunks; ++q) {
-                    const int32_t tq = t - 32 * q;
-                    s[q] = (tq >= 0) ? ld_relaxed(states + tq * kStateStride) : kFlagPrefix;   // empty prefix before tile 0
-                }
-                bool pending = false, found = false;
-                uint32_t sum = 0;
-#pragma unroll
-                for (int q = 0; q < kCompactLookChunks; ++q) {
-                    if (!found && !pending) {
-                        const uint32_t flag = s[q] & ~kValueMask;
-                        const uint32_t pmask = __ballot_sync(kFullMask, flag == kFlagPrefix);
-                        const uint32_t zmask = __ballot_sync(kFullMask, flag == 0);
-                        // lanes up to and including the nearest published prefix matter
-                        const uint32_t need = pmask ? (((pmask & (0u - pmask)) << 1) - 1u) : kFullMask;
-                        if (zmask & need) {
-                            pending = true;
-                        } else {
-                            sum += __reduce_add_sync(kFullMask, ((need >> lane) & 1u) ? (s[q] & kValueMask) : 0u);
-                            found = pmask != 0;
-                        }
-                    }
-                }
-                if (pending) {
-                    ++polls;
-                    const bool give_up = __any_sync(kFullMask, polls >= spin_limit ||
-                                                                   ld_relaxed(abort_flag) != 0);
-                    if (give_up) { ok = false; break; }
-                    backoff(ns);
-                    continue;   // re-read the whole window
-                }
-                prefix += sum;
-                if (found) break;
-                t -= 32 * kCompactLookChunks;
-            }
-            if (ok && lane == 0) st_relaxed(states + tile * kStateStride, kFlagPrefix | (prefix + total));
-        }
+        // publish the tile count at once, then look back over 32 predecessors per round
+        bool ok;
+        const uint32_t prefix = warp_look_back(states, kStateStride, tile, total, stall_tile,
+                                               spin_limit, abort_flag, ok);
         if (lane == 0) {
             s_misc[1] = ok ? 0u : 1u;
             s_misc[3] = prefix;

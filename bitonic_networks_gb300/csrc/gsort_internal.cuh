@@ -235,6 +235,46 @@ int launch_compact(const CompactLaunch &L);
 int launch_segmented_bitonic(uint32_t *keys, int64_t num_segments, int segment_len,
                              cudaStream_t stream);
 
+// 2-way split (split.cu): partition by a predicate, and the 1-bit split sort.
+struct SplitLayout {
+    uint32_t tiles;
+    size_t states_a, states_b;   // one look-back word per tile, 128 bytes apart; b: sort only
+    size_t tmp_keys, tmp_vals;   // sort only
+    size_t total;
+};
+SplitLayout split_layout(uint32_t n, bool with_values, bool sort);
+
+struct PartitionLaunch {
+    const uint32_t *in;
+    uint32_t *out;
+    const uint32_t *vals_in;   // null: no values
+    uint32_t *vals_out;
+    uint32_t n;
+    int pred, kind;
+    uint32_t param;
+    const uint8_t *flags;
+    int64_t *num_true;         // may be null
+    unsigned char *ws;
+    uint32_t spin_limit;
+    cudaStream_t stream;
+    int sm_count;
+};
+int launch_partition(const PartitionLaunch &L);
+
+struct SplitSortLaunch {
+    const uint32_t *keys_in;
+    uint32_t *keys_out;
+    const uint32_t *vals_in;
+    uint32_t *vals_out;
+    uint32_t n;
+    int begin_bit, end_bit;
+    unsigned char *ws;
+    uint32_t spin_limit;
+    cudaStream_t stream;
+    int sm_count;
+};
+int launch_split_sort(const SplitSortLaunch &L);
+
 // Variable-length segmented sort (segsort.cu): workspace layout and launch.
 struct SegLayout {
     uint32_t small_max;   // segments of 2..1024 keys, at most

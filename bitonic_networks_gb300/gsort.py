@@ -250,6 +250,85 @@ def segmented_sort(keys: torch.Tensor, offsets: torch.Tensor, values: torch.Tens
     return ko, vo
 
 
+PRED_FLAGS, PRED_BIT_SET, PRED_BIT_CLEAR, PRED_LESS, PRED_POSITIVE = 0, 1, 2, 3, 4
+
+
+def partition(x: torch.Tensor, values: torch.Tensor | None = None, *, pred: int = PRED_BIT_SET,
+              param: int = 0, kind: int = KEY_U32, flags: torch.Tensor | None = None,
+              out: torch.Tensor | None = None, values_out: torch.Tensor | None = None,
+              workspace: torch.Tensor | None = None, check: bool = True):
+    """Stable 2-way split of 32-bit elements: those whose predicate holds
+    first, the others after, each side in input order.  Returns (out,
+    values_out or None, num_true) with num_true a one-element int64 tensor."""
+    if not x.is_cuda:
+        raise ValueError("partition takes CUDA tensors")
+    xi = _flat_cuda(x, "x")
+    if xi.element_size() != 4:
+        raise TypeError("partition takes 32-bit elements")
+    v = None
+    if values is not None:
+        v = _flat_cuda(values, "values")
+        if v.numel() != xi.numel() or v.element_size() != 4:
+            raise ValueError("values must be a 32-bit tensor with one entry per element")
+    fl = None
+    if pred == PRED_FLAGS:
+        if flags is None:
+            raise ValueError("PRED_FLAGS needs flags")
+        fl = _flat_cuda(flags, "flags")
+        if fl.element_size() != 1 or fl.numel() != xi.numel():
+            raise ValueError("flags must be a 1-byte tensor with one entry per element")
+    n = xi.numel()
+    o = torch.empty_like(xi) if out is None else _flat_cuda(out, "out")
+    vo = None
+    if v is not None:
+        vo = torch.empty_like(v) if values_out is None else _flat_cuda(values_out, "values_out")
+    nt = torch.empty(1, dtype=torch.int64, device=xi.device)
+    lib = _lib.load()
+    ws = _workspace(int(lib.gsort_partition_workspace_bytes(n)), xi.device, workspace)
+    with torch.cuda.device(xi.device):
+        rc = lib.gsort_partition(xi.data_ptr(), o.data_ptr(), v.data_ptr() if v is not None else None,
+                                 vo.data_ptr() if vo is not None else None, n, pred, kind,
+                                 int(param) & 0xFFFFFFFF, fl.data_ptr() if fl is not None else None,
+                                 nt.data_ptr(), ws.data_ptr(), ws.numel(), _stream(xi.device))
+        _check(rc, "gsort_partition")
+        if check and n > 0:
+            _check(lib.gsort_check(ws.data_ptr(), _stream(xi.device)), "gsort_partition (device)")
+    o = o.view(x.shape) if out is None else out
+    if vo is not None:
+        vo = vo.view(values.shape) if values_out is None else values_out
+    return o, vo, nt
+
+
+def split_sort(keys: torch.Tensor, values: torch.Tensor | None = None, begin_bit: int = 0,
+               end_bit: int = 32, *, keys_out: torch.Tensor | None = None,
+               values_out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+               check: bool = True):
+    """The 1-bit split LSD sort (one stable split per bit) of unsigned 32-bit keys."""
+    if not keys.is_cuda:
+        raise ValueError("split_sort takes CUDA tensors")
+    k = _flat_cuda(keys, "keys")
+    v = None if values is None else _flat_cuda(values, "values")
+    n = k.numel()
+    ko = torch.empty_like(k) if keys_out is None else _flat_cuda(keys_out, "keys_out")
+    vo = None
+    if v is not None:
+        vo = torch.empty_like(v) if values_out is None else _flat_cuda(values_out, "values_out")
+    lib = _lib.load()
+    ws = _workspace(int(lib.gsort_split_sort_workspace_bytes(n, 1 if v is not None else 0)),
+                    k.device, workspace)
+    with torch.cuda.device(k.device):
+        rc = lib.gsort_split_sort(k.data_ptr(), ko.data_ptr(), v.data_ptr() if v is not None else None,
+                                  vo.data_ptr() if vo is not None else None, n, begin_bit, end_bit,
+                                  ws.data_ptr(), ws.numel(), _stream(k.device))
+        _check(rc, "gsort_split_sort")
+        if check and n > 0 and begin_bit < end_bit:
+            _check(lib.gsort_check(ws.data_ptr(), _stream(k.device)), "gsort_split_sort (device)")
+    ko = ko.view(keys.shape) if keys_out is None else keys_out
+    if vo is not None:
+        vo = vo.view(values.shape) if values_out is None else values_out
+    return ko, vo
+
+
 def sort_keys(keys: torch.Tensor, **kw) -> torch.Tensor:
     """Ascending sort of 32-bit keys (all 32 bits)."""
     if not keys.is_cuda:

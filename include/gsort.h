@@ -212,6 +212,58 @@ int gsort_segmented_bitonic(uint32_t *d_keys, int64_t num_segments,
                             int segment_len, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Stable 2-way split (partition)  ([CUDA3] "Radix Sort": predicate,
+ * exclusive scan, scatter of one side before the other; "Stream
+ * Compaction" keeps only one side)
+ *
+ * Writes every element whose predicate holds, in input order, to
+ * d_out[0..m) and every other element, in input order, to d_out[m..n);
+ * values (optional, 32-bit) move with their elements; *d_num_true = m
+ * (device int64, may be NULL).  d_in/d_vals_in must not overlap the outputs.
+ * Predicates on the 32-bit word x of element i:
+ *   GSORT_PRED_FLAGS       d_flags[i] != 0 (uint8 array of n entries)
+ *   GSORT_PRED_BIT_SET     bit `param` of x is 1 (param < 32)
+ *   GSORT_PRED_BIT_CLEAR   bit `param` of x is 0
+ *   GSORT_PRED_LESS        x < param in the sort order of `kind` (U32, I32,
+ *                          F32: IEEE totalOrder, so -0.0 < +0.0 and NaNs
+ *                          fall outside +-inf, as in the radix sort)
+ *   GSORT_PRED_POSITIVE    IEEE x > 0 for float bits (the compaction
+ *                          predicate; NaN, +0 and -0 are false)
+ * Traffic: one counting read, then one read and one write per element.
+ * ---------------------------------------------------------------------- */
+#define GSORT_PRED_FLAGS 0
+#define GSORT_PRED_BIT_SET 1
+#define GSORT_PRED_BIT_CLEAR 2
+#define GSORT_PRED_LESS 3
+#define GSORT_PRED_POSITIVE 4
+
+size_t gsort_partition_workspace_bytes(int64_t n);
+
+int gsort_partition(const uint32_t *d_in, uint32_t *d_out, const uint32_t *d_vals_in,
+                    uint32_t *d_vals_out, int64_t n, int pred, int kind, uint32_t param,
+                    const uint8_t *d_flags, int64_t *d_num_true, void *d_ws, size_t ws_bytes,
+                    cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * 1-bit split radix sort  ([CUDA3] "Radix Sort": one predicate / scan /
+ * scatter pass per bit, zeros before ones)
+ *
+ * Stable ascending sort of unsigned 32-bit keys (and 32-bit values) by the
+ * bits [begin_bit, end_bit), one split pass per bit (up to 32): the pages'
+ * bitwise LSD sort.  The zero count of every bit comes from one upfront
+ * histogram read.  Same result as gsort_radix_pairs with GSORT_KEY_U32, at
+ * about 8x its traffic; it exists as the pages' method and as a check of
+ * the split primitive.  In place and aliasing rules as for
+ * gsort_radix_pairs.
+ * ---------------------------------------------------------------------- */
+size_t gsort_split_sort_workspace_bytes(int64_t n, int with_values);
+
+int gsort_split_sort(const uint32_t *d_keys_in, uint32_t *d_keys_out,
+                     const uint32_t *d_vals_in, uint32_t *d_vals_out, int64_t n,
+                     int begin_bit, int end_bit, void *d_ws, size_t ws_bytes,
+                     cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * Variable-length segmented sort  ([PMPP10] 10.5, strategy 2: radix sort
  * for the coarse order with bitonic networks for the small pieces;
  * [GPUSORT]: pieces of <= 1024 keys go to a bitonic sort)

@@ -402,6 +402,90 @@ int oracle_segmented_sort_general(const uint32_t *keys_in, const uint32_t *vals_
 }
 
 /* ---------------------------------------------------------------------------
+ * NEXT (f3): stable 2-way split and the 1-bit split sort ([CUDA3] "Radix
+ * Sort": per bit a predicate, a scan and a scatter of the zeros before the
+ * ones).  oracle_partition copies the elements whose predicate holds, in
+ * input order, then the others, in input order, and returns their count.
+ * Predicates (pred): 0 flags[i] != 0; 1 bit `param` set; 2 bit `param`
+ * clear; 3 x before param in the sort order of `kind` (the ordered values of
+ * f1 compared); 4 x > 0 as a float (C comparison).
+ * ------------------------------------------------------------------------- */
+static int pred_holds(uint32_t x, int64_t i, int pred, int kind, uint32_t param,
+                      const uint8_t *flags)
+{
+    switch (pred) {
+    case 0: return flags[i] != 0;
+    case 1: return ((x >> param) & 1u) == 1u;
+    case 2: return ((x >> param) & 1u) == 0u;
+    case 3: return oracle_key_to_ordered(x, kind, 0) < oracle_key_to_ordered(param, kind, 0);
+    default: {
+        float f;
+        memcpy(&f, &x, sizeof(f));
+        return f > 0.0f;
+    }
+    }
+}
+
+int64_t oracle_partition(const uint32_t *in, const uint32_t *vals_in, uint32_t *out,
+                         uint32_t *vals_out, int64_t n, int pred, int kind, uint32_t param,
+                         const uint8_t *flags)
+{
+    int with_vals = (vals_in != NULL && vals_out != NULL);
+    int64_t m = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        if (pred_holds(in[i], i, pred, kind, param, flags)) {
+            out[m] = in[i];
+            if (with_vals)
+                vals_out[m] = vals_in[i];
+            ++m;
+        }
+    }
+    int64_t k = m;
+    for (int64_t i = 0; i < n; ++i) {
+        if (!pred_holds(in[i], i, pred, kind, param, flags)) {
+            out[k] = in[i];
+            if (with_vals)
+                vals_out[k] = vals_in[i];
+            ++k;
+        }
+    }
+    return m;
+}
+
+/* One stable split per bit b in [begin_bit, end_bit), zeros first. */
+int oracle_split_sort(const uint32_t *keys_in, const uint32_t *vals_in, uint32_t *keys_out,
+                      uint32_t *vals_out, int64_t n, int begin_bit, int end_bit)
+{
+    if (n < 0 || begin_bit < 0 || end_bit > 32 || begin_bit > end_bit)
+        return ORACLE_EINVAL;
+    int with_vals = (vals_in != NULL && vals_out != NULL);
+    uint32_t *x = malloc(sizeof(uint32_t) * (size_t)(n > 0 ? n : 1));
+    uint32_t *y = malloc(sizeof(uint32_t) * (size_t)(n > 0 ? n : 1));
+    uint32_t *vx = malloc(sizeof(uint32_t) * (size_t)(n > 0 ? n : 1));
+    uint32_t *vy = malloc(sizeof(uint32_t) * (size_t)(n > 0 ? n : 1));
+    if (!x || !y || !vx || !vy) {
+        free(x); free(y); free(vx); free(vy);
+        return ORACLE_ENOMEM;
+    }
+    for (int64_t i = 0; i < n; ++i) {
+        x[i] = keys_in[i];
+        vx[i] = with_vals ? vals_in[i] : 0u;
+    }
+    for (int b = begin_bit; b < end_bit; ++b) {
+        oracle_partition(x, vx, y, vy, n, 2, 0, (uint32_t)b, NULL);
+        uint32_t *t = x; x = y; y = t;
+        t = vx; vx = vy; vy = t;
+    }
+    for (int64_t i = 0; i < n; ++i) {
+        keys_out[i] = x[i];
+        if (with_vals)
+            vals_out[i] = vx[i];
+    }
+    free(x); free(y); free(vx); free(vy);
+    return ORACLE_OK;
+}
+
+/* ---------------------------------------------------------------------------
  * a4: stream compaction, the 1-bit special case ([CUDA3] "Stream
  * Compaction": predicate, exclusive scan of the predicate, scatter).  Keeps
  * every x > 0 in input order at out[0..m), writes +0.0 to out[m..n), and

@@ -108,6 +108,9 @@ class Oracle:
                                              _int, _int, _int, _int]),
         "oracle_segmented_sort_general": (_int, [_u32p, _u32p, _u32p, _u32p, _i64, _u32p, _i64,
                                                  _int, _int]),
+        "oracle_partition": (_i64, [_u32p, _u32p, _u32p, _u32p, _i64, _int, _int, ctypes.c_uint32,
+                                    ctypes.c_void_p]),
+        "oracle_split_sort": (_int, [_u32p, _u32p, _u32p, _u32p, _i64, _int, _int]),
     }
 
     def __init__(self, path: str):
@@ -232,6 +235,37 @@ class Oracle:
         _check(self.lib.oracle_segmented_sort_general(
             _ptr(k.view(np.uint32)), _ptr(v), _ptr(ko.view(np.uint32)), _ptr(vo), k.size, _ptr(off),
             max(off.size - 1, 0), kind, int(descending)), "segmented_sort_general")
+        return ko, vo
+
+    # f3: 2-way split ---------------------------------------------------
+    def partition(self, x, vals=None, pred: int = 1, kind: int = 0, param: int = 0, flags=None):
+        """(out, vals_out or None, m) with out keeping the input dtype."""
+        src_dtype = np.asarray(x).dtype
+        xi = _as_u32(x).ravel()
+        out = np.empty_like(xi)
+        v = vo = None
+        if vals is not None:
+            v = _as_u32(vals).ravel()
+            vo = np.empty_like(v)
+        fl = None
+        if flags is not None:
+            fl = np.ascontiguousarray(flags, dtype=np.uint8).ravel()
+        m = self.lib.oracle_partition(_ptr(xi), _ptr(v), _ptr(out), _ptr(vo), xi.size, pred, kind,
+                                      int(param) & 0xFFFFFFFF,
+                                      None if fl is None else fl.ctypes.data)
+        if src_dtype in (np.float32, np.int32):
+            out = out.view(src_dtype)
+        return out, vo, int(m)
+
+    def split_sort(self, keys, vals=None, begin_bit: int = 0, end_bit: int = 32):
+        k = _as_u32(keys).ravel()
+        ko = np.empty_like(k)
+        v = vo = None
+        if vals is not None:
+            v = _as_u32(vals).ravel()
+            vo = np.empty_like(v)
+        _check(self.lib.oracle_split_sort(_ptr(k), _ptr(v), _ptr(ko), _ptr(vo), k.size, begin_bit,
+                                          end_bit), "split_sort")
         return ko, vo
 
     # a4 -----------------------------------------------------------------

@@ -142,6 +142,32 @@ def test_segmented_sort_argument_errors(lib):
     assert ws(1 << 20, 1, 1) > ws(1 << 20, 1, 0) > 4 * (1 << 20)
 
 
+def test_partition_and_split_sort_argument_errors(lib):
+    big = 1 << 40
+    F = 0x50000000
+    p = lib.gsort_partition
+    assert p(A, B, None, None, 0, 1, 0, 3, None, None, W, big, None) == 0         # n == 0 (no num_true)
+    assert p(A, B, None, None, -1, 1, 0, 3, None, None, W, big, None) == EINVAL
+    assert p(A, B, None, None, 10, 5, 0, 3, None, None, W, big, None) == EINVAL   # no such predicate
+    assert p(A, B, None, None, 10, 1, 0, 32, None, None, W, big, None) == EINVAL  # bit 32
+    assert p(A, B, None, None, 10, 3, 3, 0, None, None, W, big, None) == EINVAL   # LESS on a 64-bit kind
+    assert p(A, B, None, None, 10, 0, 0, 0, None, None, W, big, None) == EINVAL   # flags missing
+    assert p(A, A + 8, None, None, 10, 1, 0, 0, None, None, W, big, None) == EINVAL   # in/out overlap
+    assert p(A, A, None, None, 10, 1, 0, 0, None, None, W, big, None) == EINVAL   # no in place
+    assert p(A, B, None, None, 10, 0, 0, 0, B + 4, None, W, big, None) == EINVAL  # flags inside out
+    assert p(A + 2, B, None, None, 10, 1, 0, 0, None, None, W, big, None) == EALIGN
+    assert p(A, B, None, None, 10, 1, 0, 0, None, W + 4, W + 0x1000, big, None) == EALIGN   # num_true
+    assert p(A, B, None, None, 10, 1, 0, 0, None, None, W, 16, None) == EWS
+    s = lib.gsort_split_sort
+    assert s(A, B, None, None, 0, 0, 32, None, 0, None) == 0
+    assert s(A, B, None, None, 10, 0, 33, W, big, None) == EINVAL
+    assert s(A, B, None, None, 10, 5, 4, W, big, None) == EINVAL
+    assert s(A, A + 4, None, None, 10, 0, 32, W, big, None) == EINVAL
+    assert s(A, B, None, None, 10, 0, 32, W, 64, None) == EWS
+    assert lib.gsort_split_sort_workspace_bytes(1 << 20, 1) > lib.gsort_split_sort_workspace_bytes(1 << 20, 0)
+    assert lib.gsort_partition_workspace_bytes(-1) == 0
+
+
 def test_launch_count(lib):
     assert lib.gsort_radix_launch_count(100, 0, 32, 0) == 6
     assert lib.gsort_radix_launch_count(100, 0, 8, 0) == 3

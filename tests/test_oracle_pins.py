@@ -586,6 +586,77 @@ def test_segmented_general_rejects_bad_offsets(orc):
     assert ko.tolist() == list(range(10))
 
 
+# ------------------------------------------------------ f3: 2-way split
+
+def _total_order_less(x, p):
+    """numpy IEEE totalOrder 'x < p' for float32 arrays without NaN."""
+    return (x < p) | ((x == p) & np.signbit(x) & ~np.signbit(np.float32(p)))
+
+
+def pin_partition_vs_numpy(orc):
+    rng = np.random.default_rng(21)
+    n = 5000
+    u = synth.uniform_keys(n, 21)
+    idx = np.arange(n, dtype=np.uint32)
+    cases = []
+    flags = (rng.random(n) < 0.3).astype(np.uint8)
+    cases.append((u, dict(pred=0, flags=flags), flags.astype(bool)))
+    for b in (0, 7, 31):
+        cases.append((u, dict(pred=1, param=b), ((u >> np.uint32(b)) & np.uint32(1)) == 1))
+        cases.append((u, dict(pred=2, param=b), ((u >> np.uint32(b)) & np.uint32(1)) == 0))
+    piv = int(u[17])
+    cases.append((u, dict(pred=3, kind=0, param=piv), u < np.uint32(piv)))
+    s32 = u.view(np.int32)
+    cases.append((s32, dict(pred=3, kind=2, param=int(np.uint32(s32[5].view(np.uint32)))), s32 < s32[5]))
+    f = synth.normal_f32_with_specials(n, 22)
+    for pv in (0.0, -0.0, 0.5, -np.inf):
+        pbits = int(np.float32(pv).view(np.uint32))
+        cases.append((f, dict(pred=3, kind=1, param=pbits), _total_order_less(f, np.float32(pv))))
+    cases.append((f, dict(pred=4), f > 0))
+    for x, kw, mask in cases:
+        out, vo, m = orc.partition(x, idx, **kw)
+        assert m == int(mask.sum()), kw
+        exp = np.concatenate([idx[mask], idx[~mask]])
+        assert np.array_equal(vo, exp), kw
+        assert np.array_equal(np.asarray(out).view(np.uint32), np.asarray(x).view(np.uint32)[exp]), kw
+
+
+def pin_partition_worked_example(orc):
+    g = load_golden("compaction_worked_example.txt")
+    x = _f32(g["input"])
+    out, _, m = orc.partition(x, None, pred=4)
+    kept = int(g["kept"][0])
+    assert m == kept
+    assert np.array_equal(_bits(out[:m]), _bits(_f32(g["expected"])[:kept]))
+
+
+def pin_split_sort(orc):
+    rng = np.random.default_rng(23)
+    keys = synth.uniform_keys(3000, 23)
+    keys[::5] = keys[1::5][: keys[::5].size]
+    idx = np.arange(keys.size, dtype=np.uint32)
+    for b, e in [(0, 32), (3, 17), (31, 32), (0, 1), (8, 24)]:
+        ko, vo = orc.split_sort(keys, idx, b, e)
+        mask = (1 << (e - b)) - 1
+        exp = sorted(range(keys.size), key=lambda i: (int(keys[i]) >> b) & mask)
+        assert vo.tolist() == exp, (b, e)
+        assert np.array_equal(ko, keys[exp])
+        k8, v8 = orc.radix_sort_pairs(keys, idx, 0, b, e)     # the 8-bit oracle agrees
+        assert np.array_equal(ko, k8) and np.array_equal(vo, v8)
+
+
+def test_partition_vs_numpy(orc):
+    pin_partition_vs_numpy(orc)
+
+
+def test_partition_worked_example(orc):
+    pin_partition_worked_example(orc)
+
+
+def test_split_sort(orc):
+    pin_split_sort(orc)
+
+
 MUTANTS = {
     # a reversed scatter: each pass is no longer stable
     "unstable_scatter": ("for (int64_t i = 0; i < n; ++i) {\n            uint32_t d = digit_of",
@@ -619,6 +690,11 @@ MUTANTS = {
     # f2: the last segment is left unsorted
     "segmented_last": ("for (int64_t s = 0; s < num_segments; ++s) {\n        uint32_t a = offsets[s];",
                        "for (int64_t s = 0; s + 1 < num_segments; ++s) {\n        uint32_t a = offsets[s];"),
+    # f3: the false side of a split in reverse order
+    "partition_false_reversed": ("    int64_t k = m;\n    for (int64_t i = 0; i < n; ++i) {",
+                                 "    int64_t k = m;\n    for (int64_t i = n - 1; i >= 0; --i) {"),
+    # f3: bit test of the wrong bit
+    "partition_bit": ("case 1: return ((x >> param) & 1u) == 1u;", "case 1: return ((x >> (param + 1)) & 1u) == 1u;"),
     "descending_width": ("    }\n    if (descending)\n        u = (w == 64 ? 0xFFFFFFFFFFFFFFFFull : 0xFFFFFFFFull) - u;",
                          "    }\n    if (descending)\n        u = 0xFFFFFFFFull - u;"),
 }
@@ -628,7 +704,8 @@ PINS = [pin_radix_worked_example, pin_compaction_worked_example, pin_bitonic_exe
         pin_sort_vs_python_sorted, pin_float_sort_vs_python_sorted,
         pin_compaction_specials, pin_bitonic_zero_one, pin_segmented_vs_numpy,
         pin_general_vs_python_sorted, pin_general_bit_range, pin_general_maps,
-        pin_segmented_general]
+        pin_segmented_general, pin_partition_vs_numpy, pin_partition_worked_example,
+        pin_split_sort]
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
