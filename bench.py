@@ -465,6 +465,88 @@ def rows(lib, gsort, synth, device, stream, args, peak):
     gbs = 8 * n / (ms * 1e-3) / 1e9
     out["compact_f32_2^28"] = {"n": n, "ms": ms, "Gkeys/s": n / (ms * 1e-3) / 1e9, "GB/s": gbs,
                                "frac": gbs / peak}
+    del x, o, ws
+    torch.cuda.empty_cache()
+
+    # next rows: 64-bit keys, variable-length segments, 2-way split, 1-bit split sort
+    w = synth.WORKLOADS["uniform_u64_2^27"]
+    n = w["n"]
+    k = torch.from_numpy(synth.make_keys(w["gen"], n, w["seed"]).view(np.int64)).to(device)
+    ko = torch.empty_like(k)
+    ws = torch.empty(lib.gsort_radix_sort_workspace_bytes(n, 3, 0), dtype=torch.uint8, device=device)
+
+    def u64_fn():
+        assert lib.gsort_radix_sort(k.data_ptr(), ko.data_ptr(), None, None, n, 3, 0, 0, 64,
+                                    ws.data_ptr(), ws.numel(), stream.cuda_stream) == 0
+    ms = _median_ms(u64_fn, stream, warm, reps)
+    assert lib.gsort_check(ws.data_ptr(), stream.cuda_stream) == 0
+    byts = 16 * 8 * n
+    out["uniform_u64_2^27"] = {"n": n, "ms": ms, "Gkeys/s": n / (ms * 1e-3) / 1e9,
+                               "GB/s": byts / (ms * 1e-3) / 1e9,
+                               "frac": byts / (ms * 1e-3) / 1e9 / peak, "bytes": byts}
+    del k, ko, ws
+    torch.cuda.empty_cache()
+
+    w = synth.WORKLOADS["segments_mixed_2^26"]
+    n = w["n"]
+    k = dev(synth.make_keys(w["gen"], n, w["seed"]))
+    off_np = synth.segment_offsets(n, w["mix"], w["seed"])
+    off = dev(off_np)
+    ko = torch.empty_like(k)
+    S = off_np.size - 1
+    ws = torch.empty(lib.gsort_segmented_sort_workspace_bytes(n, S, 0), dtype=torch.uint8,
+                     device=device)
+
+    def seg_var_fn():
+        assert lib.gsort_segmented_sort(k.data_ptr(), ko.data_ptr(), None, None, n, off.data_ptr(),
+                                        S, 0, 0, ws.data_ptr(), ws.numel(), stream.cuda_stream) == 0
+    ms = _median_ms(seg_var_fn, stream, warm, reps)
+    assert lib.gsort_check(ws.data_ptr(), stream.cuda_stream) == 0
+    lens = np.diff(off_np.astype(np.int64))
+    n_small = int(lens[lens <= 1024].sum())
+    byts = 8 * n_small + 32 * (n - n_small)   # one read + write for short segments, 4 passes for long
+    out["segments_mixed_2^26"] = {"n": n, "segments": S, "keys_in_short_segments": n_small,
+                                  "ms": ms, "Gkeys/s": n / (ms * 1e-3) / 1e9,
+                                  "GB/s": byts / (ms * 1e-3) / 1e9,
+                                  "frac": byts / (ms * 1e-3) / 1e9 / peak, "bytes": byts}
+    del k, ko, off, ws
+    torch.cuda.empty_cache()
+
+    w = synth.WORKLOADS["partition_f32_2^28"]
+    n = w["n"]
+    x = dev(synth.make_keys(w["gen"], n, w["seed"]))
+    o = torch.empty_like(x)
+    nt = torch.empty(1, dtype=torch.int64, device=device)
+    ws = torch.empty(lib.gsort_partition_workspace_bytes(n), dtype=torch.uint8, device=device)
+
+    def part_fn():
+        assert lib.gsort_partition(x.data_ptr(), o.data_ptr(), None, None, n, 4, 1, 0, None,
+                                   nt.data_ptr(), ws.data_ptr(), ws.numel(), stream.cuda_stream) == 0
+    ms = _median_ms(part_fn, stream, warm, reps)
+    assert lib.gsort_check(ws.data_ptr(), stream.cuda_stream) == 0
+    byts = 8 * n
+    out["partition_f32_2^28"] = {"n": n, "ms": ms, "Gkeys/s": n / (ms * 1e-3) / 1e9,
+                                 "GB/s": byts / (ms * 1e-3) / 1e9,
+                                 "frac": byts / (ms * 1e-3) / 1e9 / peak, "bytes": byts,
+                                 "note": "bytes = one read and one write; the counting read adds 4 B/element"}
+    del x, o, ws
+    torch.cuda.empty_cache()
+
+    w = synth.WORKLOADS["split_sort_u32_2^25"]
+    n = w["n"]
+    k = dev(synth.make_keys(w["gen"], n, w["seed"]))
+    ko = torch.empty_like(k)
+    ws = torch.empty(lib.gsort_split_sort_workspace_bytes(n, 0), dtype=torch.uint8, device=device)
+
+    def split_fn():
+        assert lib.gsort_split_sort(k.data_ptr(), ko.data_ptr(), None, None, n, 0, 32,
+                                    ws.data_ptr(), ws.numel(), stream.cuda_stream) == 0
+    ms = _median_ms(split_fn, stream, warm, reps)
+    assert lib.gsort_check(ws.data_ptr(), stream.cuda_stream) == 0
+    byts = 8 * 32 * n
+    out["split_sort_u32_2^25"] = {"n": n, "ms": ms, "Gkeys/s": n / (ms * 1e-3) / 1e9,
+                                  "GB/s": byts / (ms * 1e-3) / 1e9,
+                                  "frac": byts / (ms * 1e-3) / 1e9 / peak, "bytes": byts}
     return out
 
 

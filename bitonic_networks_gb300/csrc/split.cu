@@ -50,13 +50,46 @@ struct PredPositive {       // IEEE x > 0 on the bit pattern (0 < bits <= 0x7F80
 };
 
 // --------------------------------------------------------------- counting
+// Grid-stride count of the elements whose predicate holds: 16-byte loads,
+// four in flight per thread (a flags predicate reads 4 flag bytes per group
+// of 4 elements instead of the words).  vec: the source is suitably aligned
+// (16 bytes for words, 4 for flags); otherwise one element at a time.
+template <class Pred> struct PredReadsFlags { static constexpr bool value = false; };
+template <> struct PredReadsFlags<PredFlags> { static constexpr bool value = true; };
+
+template <class Pred>
+__device__ __forceinline__ uint32_t count_group(const uint32_t *in, const Pred &pred, uint32_t g) {
+    // elements g .. g+3
+    if constexpr (PredReadsFlags<Pred>::value) {
+        const uint32_t f = *reinterpret_cast<const uint32_t *>(pred.flags + g);
+        return ((f & 0xFFu) != 0) + ((f & 0xFF00u) != 0) + ((f & 0xFF0000u) != 0) + ((f >> 24) != 0);
+    } else {
+        const uint4 q = __ldcs(reinterpret_cast<const uint4 *>(in + g));
+        return pred.test(q.x, g) + pred.test(q.y, g + 1) + pred.test(q.z, g + 2) + pred.test(q.w, g + 3);
+    }
+}
+
 template <class Pred>
 __global__ void __launch_bounds__(256)
-k_count_true(const uint32_t *__restrict__ in, uint32_t n, Pred pred, uint32_t *total) {
+k_count_true(const uint32_t *__restrict__ in, uint32_t n, Pred pred, uint32_t *total, int vec) {
+    constexpr int U = 4;
     __shared__ uint32_t s_w[8];
+    const uint32_t gtid = blockIdx.x * blockDim.x + threadIdx.x;
+    const uint32_t gstride = gridDim.x * blockDim.x;
     uint32_t c = 0;
-    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
-        c += pred.test(in[i], i) ? 1u : 0u;
+    const uint32_t groups = vec ? n / 4 : 0;
+    for (uint32_t q = gtid; q < groups; q += U * gstride) {
+        uint32_t part[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t qq = q + u * gstride;
+            part[u] = qq < groups ? count_group(in, pred, 4 * qq) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) c += part[u];
+    }
+    for (uint32_t i = 4 * groups + gtid; i < n; i += gstride)   // the tail, or everything when !vec
+        c += pred.test(PredReadsFlags<Pred>::value ? 0u : in[i], i) ? 1u : 0u;
     c = __reduce_add_sync(kFullMask, c);
     if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = c;
     __syncthreads();
@@ -86,7 +119,7 @@ k_split(const uint32_t *__restrict__ in, const uint32_t *__restrict__ vin, uint3
         uint32_t *abort_flag, uint32_t spin_limit, uint32_t stall_tile, int vec_ok) {
     constexpr int T = kSplitThreads, IPT = kSplitItems, WARPS = T / 32;
     constexpr uint32_t TILE = kSplitTile;
-    extern __shared__ __align__(16) uint32_t smem[];
+    extern __shared__ __align__(128) uint32_t smem[];
     uint32_t *s_buf = smem;                    // [TILE] true run, then false run
     uint32_t *s_vbuf = smem + TILE;            // [TILE] their values (pairs)
     __shared__ uint32_t s_warp[WARPS];
@@ -224,8 +257,11 @@ cudaError_t launch_split_any(bool pairs, const uint32_t *in, const uint32_t *vin
 template <class Pred>
 cudaError_t launch_count(const uint32_t *in, uint32_t n, const Pred &pred, uint32_t *total,
                          int sm_count, cudaStream_t s) {
-    const uint32_t grid = std::max(1u, std::min((n + 255) / 256, static_cast<uint32_t>(sm_count) * 8));
-    k_count_true<Pred><<<grid, 256, 0, s>>>(in, n, pred, total);
+    int vec;
+    if constexpr (PredReadsFlags<Pred>::value) vec = (reinterpret_cast<uintptr_t>(pred.flags) & 3) == 0;
+    else vec = (reinterpret_cast<uintptr_t>(in) & 15) == 0;
+    const uint32_t grid = std::max(1u, std::min((n / 4 + 255) / 256, static_cast<uint32_t>(sm_count) * 8));
+    k_count_true<Pred><<<grid, 256, 0, s>>>(in, n, pred, total, vec);
     return cudaGetLastError();
 }
 

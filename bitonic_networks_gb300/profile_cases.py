@@ -7,7 +7,9 @@ OP: keys (uint32 keys, 32 bits), pairs (uint32 key/index pairs), fpairs
 (float keys with index values), compact (compaction input), segments (1024-key
 segments, n/1024 of them), hist (the digit-histogram step alone), sort (any
 key kind: --kind u32|f32|i32|u64|f64|i64 [--desc] [--values]), segsort
-(variable-length segments, --mix small|mixed|large [--values] [--desc]).
+(variable-length segments, --mix small|mixed|large [--values] [--desc]),
+partition (compaction input split by x > 0 [--values]), splitsort (the 1-bit
+split sort of uint32 keys [--values]).
 --time prints the median CUDA-event time of the timed calls.
 Each call is followed by a device-status check; the process exits non-zero on
 any error, so a profiler only ever runs a command that finished cleanly.
@@ -26,7 +28,7 @@ from . import _lib, gsort, synth
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("op", choices=["keys", "pairs", "fpairs", "compact", "segments", "hist", "sort",
-                                   "segsort"])
+                                   "segsort", "partition", "splitsort"])
     ap.add_argument("--mix", choices=["small", "mixed", "large"], default="mixed")
     ap.add_argument("--kind", choices=["u32", "f32", "i32", "u64", "f64", "i64"], default="u64")
     ap.add_argument("--desc", action="store_true")
@@ -46,7 +48,13 @@ def main(argv=None) -> int:
 
     kinds = {"u32": 0, "f32": 1, "i32": 2, "u64": 3, "f64": 4, "i64": 5}
     kind = kinds[a.kind]
-    if a.op == "segsort":
+    if a.op == "partition":
+        x = up(synth.compaction_input(n, 9))
+        v = up(synth.index_values(n)) if a.values else None
+    elif a.op == "splitsort":
+        x = up(synth.uniform_keys(n, 10))
+        v = up(synth.index_values(n)) if a.values else None
+    elif a.op == "segsort":
         x = up(synth.uniform_keys(n, 7))
         off_np = synth.segment_offsets(n, a.mix, 8)
         off = up(off_np)
@@ -72,7 +80,11 @@ def main(argv=None) -> int:
         x = seg.clone()
 
     def once():
-        if a.op == "segsort":
+        if a.op == "partition":
+            gsort.partition(x, v, pred=gsort.PRED_POSITIVE, check=not a.time)
+        elif a.op == "splitsort":
+            gsort.split_sort(x, v, 0, 32, check=not a.time)
+        elif a.op == "segsort":
             gsort.segmented_sort(x, off, v, descending=a.desc, kind=0, check=not a.time)
         elif a.op == "sort":
             gsort.sort(x, v, descending=a.desc, kind=kind, check=not a.time)

@@ -222,6 +222,12 @@ WORKLOADS = {
     "segments_16384x1024": dict(kind="segments", n=16384 * 1024, segments=16384, length=1024,
                                 gen="uniform", seed=SEED_BASE + 6),
     "compact_f32_2^28": dict(kind="compact", n=1 << 28, gen="compaction", seed=SEED_BASE + 7),
+    # the "next" rows: other key kinds, variable-length segments, 2-way split
+    "uniform_u64_2^27": dict(kind="u64", n=1 << 27, gen="keys64", seed=SEED_BASE + 8),
+    "segments_mixed_2^26": dict(kind="segsort", n=1 << 26, gen="uniform", mix="mixed",
+                                seed=SEED_BASE + 9),
+    "partition_f32_2^28": dict(kind="partition", n=1 << 28, gen="compaction", seed=SEED_BASE + 10),
+    "split_sort_u32_2^25": dict(kind="splitsort", n=1 << 25, gen="uniform", seed=SEED_BASE + 11),
 }
 
 
@@ -236,4 +242,6 @@ def make_keys(gen: str, n: int, seed: int) -> np.ndarray:
         return normal_f32_with_specials(n, seed)
     if gen == "compaction":
         return compaction_input(n, seed)
+    if gen == "keys64":
+        return keys64(n, seed)
     raise ValueError(gen)

@@ -59,3 +59,47 @@ def test_compaction_full_size():
     exp, m = oracle.compact_positive(x)
     assert int(nk.item()) == m
     assert_bits_equal(host_u32(got), exp, "compaction")
+
+
+# ---- the "next" rows at the sizes the bench rows time
+
+def test_u64_full_size():
+    w = synth.WORKLOADS["uniform_u64_2^27"]
+    k = synth.make_keys(w["gen"], w["n"], w["seed"])
+    t = torch.from_numpy(k.view(np.int64)).cuda()
+    got, _ = gsort.sort(t, kind=gsort.KEY_U64)
+    got = got.cpu().numpy().view(np.uint64)
+    del t
+    torch.cuda.empty_cache()
+    exp, _ = oracle.default().radix_sort(k, None, 3)
+    assert np.array_equal(got, exp), "u64 keys"
+
+
+def test_segments_mixed_full_size():
+    w = synth.WORKLOADS["segments_mixed_2^26"]
+    k = synth.make_keys(w["gen"], w["n"], w["seed"])
+    off = synth.segment_offsets(w["n"], w["mix"], w["seed"])
+    v = synth.index_values(w["n"])
+    ko, vo = gsort.segmented_sort(dev(k), dev(off), dev(v), kind=gsort.KEY_U32)
+    ek, ev = oracle.default().segmented_sort_general(k, off, v, 0)
+    assert_bits_equal(host_u32(ko), ek, "segmented keys")
+    assert_bits_equal(host_u32(vo), ev, "segmented values")
+
+
+def test_partition_full_size():
+    w = synth.WORKLOADS["partition_f32_2^28"]
+    x = synth.make_keys(w["gen"], w["n"], w["seed"])
+    o, _, nt = gsort.partition(dev(x), pred=gsort.PRED_POSITIVE)
+    eo, _, m = oracle.default().partition(x, None, pred=4)
+    assert int(nt.item()) == m
+    assert_bits_equal(host_u32(o), eo, "partition")
+
+
+def test_split_sort_full_size():
+    w = synth.WORKLOADS["split_sort_u32_2^25"]
+    k = synth.make_keys(w["gen"], w["n"], w["seed"])
+    v = synth.index_values(w["n"])
+    ko, vo = gsort.split_sort(dev(k), dev(v))
+    ek, ev = oracle.default().split_sort(k, v, 0, 32)
+    assert_bits_equal(host_u32(ko), ek, "split sort keys")
+    assert_bits_equal(host_u32(vo), ev, "split sort values")
