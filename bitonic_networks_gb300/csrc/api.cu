@@ -1,18 +1,91 @@
 // api.cu -- the extern "C" boundary of libgsort: argument validation,
 // workspace sizing and launch dispatch.  Validation happens before any CUDA
 // call, so every argument error is reported without touching the device.
+#include <atomic>
 #include <cstring>
+#include <mutex>
+#include <unordered_map>
 
 #include "gsort_internal.cuh"
 
 namespace gsort {
 
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];   // 0: not yet queried
+
+struct KernelKey {
+    const void *kernel;
+    int device, threads;
+    size_t smem;
+    bool operator==(const KernelKey &o) const {
+        return kernel == o.kernel && device == o.device && threads == o.threads && smem == o.smem;
+    }
+};
+struct KernelKeyHash {
+    size_t operator()(const KernelKey &k) const {
+        return std::hash<const void *>()(k.kernel) ^ (static_cast<size_t>(k.device) << 48) ^
+               (static_cast<size_t>(k.threads) << 32) ^ k.smem;
+    }
+};
+std::mutex g_cache_mutex;
+std::unordered_map<KernelKey, int, KernelKeyHash> g_smem_set;    // value unused
+std::unordered_map<KernelKey, int, KernelKeyHash> g_occupancy;
+}  // namespace
+
 int device_info(DeviceInfo *out) {
     if (cudaGetDevice(&out->device) != cudaSuccess) return GSORT_ECUDA;
+    if (out->device >= 0 && out->device < kMaxDevices) {
+        const int c = g_sm_count[out->device].load(std::memory_order_relaxed);
+        if (c > 0) {
+            out->sm_count = c;
+            return GSORT_OK;
+        }
+    }
     if (cudaDeviceGetAttribute(&out->sm_count, cudaDevAttrMultiProcessorCount, out->device) !=
         cudaSuccess)
         return GSORT_ECUDA;
+    if (out->device >= 0 && out->device < kMaxDevices)
+        g_sm_count[out->device].store(out->sm_count, std::memory_order_relaxed);
     return GSORT_OK;
+}
+
+cudaError_t set_smem_limit(const void *kernel, size_t bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const KernelKey key{kernel, dev, 0, bytes};
+    {
+        std::lock_guard<std::mutex> lock(g_cache_mutex);
+        if (g_smem_set.count(key)) return cudaSuccess;
+    }
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    if (e == cudaSuccess) {
+        std::lock_guard<std::mutex> lock(g_cache_mutex);
+        g_smem_set.emplace(key, 1);
+    }
+    return e;
+}
+
+cudaError_t blocks_per_sm(const void *kernel, int threads, size_t smem, int *out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const KernelKey key{kernel, dev, threads, smem};
+    {
+        std::lock_guard<std::mutex> lock(g_cache_mutex);
+        auto it = g_occupancy.find(key);
+        if (it != g_occupancy.end()) {
+            *out = it->second;
+            return cudaSuccess;
+        }
+    }
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, kernel, threads, smem);
+    if (e == cudaSuccess) {
+        std::lock_guard<std::mutex> lock(g_cache_mutex);
+        g_occupancy.emplace(key, *out);
+    }
+    return e;
 }
 
 namespace {
@@ -472,6 +545,8 @@ int gsort_radix_launch_count(int64_t n, int begin_bit, int end_bit, int in_place
 int gsort_radix_sort_launch_count(int64_t n, int kind, int begin_bit, int end_bit, int in_place) {
     const int kb = key_kind_bytes(kind);
     if (n <= 0 || begin_bit >= end_bit || kb == 0) return 0;
+    if (n <= GSORT_MAX_N && small_sort_applies(static_cast<uint32_t>(n), kb, 0))
+        return 2;   // header clear + one cooperative kernel for every pass
     const int passes = (end_bit - begin_bit + 7) / 8;
     return 2 + passes + ((in_place && (passes & 1)) ? 1 : 0) + (kb == 8 ? 1 : 0);
 }

@@ -149,7 +149,13 @@ struct DeviceInfo {
     int device;
     int sm_count;
 };
-int device_info(DeviceInfo *out);  // returns GSORT_OK or GSORT_ECUDA
+int device_info(DeviceInfo *out);  // returns GSORT_OK or GSORT_ECUDA; cached per device
+
+// Per-device caches of kernel properties, so that a call costs no more host
+// time than its launches: the dynamic shared-memory limit of a kernel (set
+// once per device and size) and its resident CTAs per SM.
+cudaError_t set_smem_limit(const void *kernel, size_t bytes);
+cudaError_t blocks_per_sm(const void *kernel, int threads, size_t smem, int *out);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -197,6 +203,7 @@ struct RadixLayout {
     size_t hist;          // u32[passes][256] digit histograms
     size_t look_a, look_b;  // [tiles_max][256] look-back words, alternating between passes
     size_t tmp_keys, tmp_vals;
+    size_t small_counts;  // 32-bit keys, n <= 2^18: the small-input sort's count buffers
     size_t total;
 };
 RadixLayout radix_layout(uint32_t n, bool with_values, int key_bytes);
@@ -234,6 +241,30 @@ int launch_compact(const CompactLaunch &L);
 
 int launch_segmented_bitonic(uint32_t *keys, int64_t num_segments, int segment_len,
                              cudaStream_t stream);
+
+// Small inputs (small.cu): every pass of a 32-bit key sort in one cooperative
+// launch.  launch_small_sort returns 1 (and launches nothing) when the grid
+// cannot be resident at once; the caller then takes the large-input path.
+struct SmallSortLaunch {
+    const uint32_t *keys_in;
+    uint32_t *keys_out;
+    const uint32_t *vals_in;
+    uint32_t *vals_out;
+    uint32_t *tmp_k, *tmp_v;
+    uint32_t n;
+    int passes, begin_bit;
+    uint32_t last_mask, fmask, flip;
+    bool alias;
+    uint32_t *counts;            // 3 x [ceil(n / small_sort_tile())][256]
+    uint32_t *bar_count;         // zero before the launch
+    uint32_t *status, *abort_flag;
+    uint32_t spin_limit, stall_tile;
+    cudaStream_t stream;
+    int sm_count;
+};
+bool small_sort_applies(uint32_t n, int key_bytes, int variant);
+uint32_t small_sort_tile();
+int launch_small_sort(const SmallSortLaunch &L);
 
 // 2-way split (split.cu): partition by a predicate, and the 1-bit split sort.
 struct SplitLayout {

@@ -130,11 +130,10 @@ struct PersistentConfig {
     static cudaError_t launch_one(const PassArgs &a, uint32_t tiles, cudaStream_t s) {
         auto k = k_digit_pass_persistent<WARPS, IPT, MATCH, LW, B, P, XI, XO>;
         const size_t smem = persist_smem_words<WARPS, IPT, P>() * sizeof(uint32_t);
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
+        cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(k), smem);
         if (e != cudaSuccess) return e;
         int per_sm = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, WARPS * 32, smem);
+        e = blocks_per_sm(reinterpret_cast<const void *>(k), WARPS * 32, smem, &per_sm);
         if (e != cudaSuccess) return e;
         int dev = 0, sms = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -232,6 +231,11 @@ RadixLayout radix_layout(uint32_t n, bool with_values, int key_bytes) {
     off += align_up(static_cast<size_t>(n) * key_bytes, kWsAlign);
     L.tmp_vals = off;
     if (with_values) off += align_up(static_cast<size_t>(n) * sizeof(uint32_t), kWsAlign);
+    // the one-launch sort of small inputs: three rotating [tiles][256] count buffers
+    L.small_counts = off;
+    if (small_sort_applies(n, key_bytes, 0))
+        off += align_up(3 * static_cast<size_t>((n + small_sort_tile() - 1) / small_sort_tile()) * 256 *
+                            sizeof(uint32_t), kWsAlign);
     L.total = off;
     return L;
 }
@@ -286,6 +290,38 @@ int launch_radix(const RadixLaunch &L) {
 
     const uint32_t last_width = static_cast<uint32_t>(L.end_bit - L.begin_bit - 8 * (passes - 1));
     const uint32_t last_mask = (1u << last_width) - 1u;
+    const bool alias = (L.keys_in == L.keys_out) || (pairs && L.vals_in == L.vals_out);
+
+    if (small_sort_applies(L.n, order.key_bytes, L.variant)) {
+        SmallSortLaunch S;
+        S.keys_in = static_cast<const uint32_t *>(L.keys_in);
+        S.keys_out = static_cast<uint32_t *>(L.keys_out);
+        S.vals_in = L.vals_in;
+        S.vals_out = L.vals_out;
+        S.tmp_k = static_cast<uint32_t *>(tmp_k);
+        S.tmp_v = tmp_v;
+        S.n = L.n;
+        S.passes = passes;
+        S.begin_bit = L.begin_bit;
+        S.last_mask = last_mask;
+        S.fmask = static_cast<uint32_t>(order.fmask);
+        S.flip = static_cast<uint32_t>(order.flip);
+        S.alias = alias;
+        S.counts = reinterpret_cast<uint32_t *>(L.ws + lay.small_counts);
+        S.bar_count = reinterpret_cast<uint32_t *>(L.ws + kHdrCounters + 128 * 6);
+        S.status = status;
+        S.abort_flag = abort_flag;
+        S.spin_limit = L.spin_limit;
+        S.stall_tile = L.stall_tile;
+        S.stream = s;
+        S.sm_count = L.sm_count;
+        const int rc = launch_small_sort(S);
+        if (rc != 1) {
+            for (int i = 2; i < 3 + passes; ++i) record(L.events, L.num_events, i, s);
+            return rc;
+        }
+    }
+
     // the histogram kernel also clears the first pass's look-back words
     if (launch_hist_any(L.keys_in, L.n, order, L.begin_bit, passes, last_mask, hist, look[0],
                         tiles * 256, s, L.sm_count) != cudaSuccess)
@@ -295,7 +331,6 @@ int launch_radix(const RadixLaunch &L) {
     // In place (either array): in -> tmp -> out -> tmp ...; an odd pass count
     // ends in tmp and is copied back.  Otherwise the sequence is arranged so
     // that the last pass writes to out.
-    const bool alias = (L.keys_in == L.keys_out) || (pairs && L.vals_in == L.vals_out);
     const void *src_k = L.keys_in;
     const uint32_t *src_v = L.vals_in;
     void *dst_k = nullptr;

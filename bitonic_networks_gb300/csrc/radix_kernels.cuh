@@ -562,8 +562,7 @@ struct PassConfig {
     static cudaError_t launch_one(const PassArgs &a, uint32_t tiles, cudaStream_t s) {
         auto k = k_digit_pass<K, WARPS, IPT, MINB, MATCH, LW, B, P, XI, XO>;
         const size_t smem = pass_smem_words<K, WARPS, IPT, P>() * sizeof(uint32_t);
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
+        cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(k), smem);
         if (e != cudaSuccess) return e;
         k<<<tiles, WARPS * 32, smem, s>>>(a);
         return cudaGetLastError();
@@ -606,8 +605,7 @@ cudaError_t launch_hist_kernel(const K *keys, uint32_t n, bool xf, K fmask, K fl
     auto k = xf ? (byte ? k_digit_hist<K, true, true> : k_digit_hist<K, true, false>)
                 : (byte ? k_digit_hist<K, false, true> : k_digit_hist<K, false, false>);
     const size_t smem = static_cast<size_t>(passes) * (sizeof(K) == 8 ? 128 : 256) * 32 * sizeof(uint32_t);
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kHistSmemBytes));
+    cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(k), kHistSmemBytes);
     if (e != cudaSuccess) return e;
     k<<<grid, kHistThreads, smem, s>>>(keys, n, begin_bit, passes, last_mask, fmask, flip, hist, cl,
                                        clear_words / 4);

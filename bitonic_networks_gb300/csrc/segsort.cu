@@ -239,8 +239,7 @@ struct SegPassLaunch {
         auto k = k_seg_pass<true, PAIRS, XI, XO>;
         const size_t smem = (static_cast<size_t>(kSegTile) * (PAIRS ? 2 : 1) + kSegPassWarps * kRow +
                              256 + 32) * sizeof(uint32_t);
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
+        cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(k), smem);
         if (e != cudaSuccess) return e;
         k<<<grid, kSegPassWarps * 32, smem, s>>>(a, tiles, counts, hist);
         return cudaGetLastError();
@@ -362,8 +361,7 @@ cudaError_t launch_small_class(const uint32_t *offsets, const uint32_t *small_li
     constexpr uint32_t kPadded = kLp + kLp / 32;
     const size_t smem = kSmallWarps * (kPadded * sizeof(E) + (PAIRS ? kLp * sizeof(uint32_t) : 0));
     auto k = k_seg_small<LOG_R, PAIRS, XF>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(k), smem);
     if (e != cudaSuccess) return e;
     k<<<grid, kSmallWarps * 32, smem, s>>>(offsets, small_list, counts, small_max, keys_in, keys_out,
                                            vals_in, vals_out, fmask, flip, abort_flag);

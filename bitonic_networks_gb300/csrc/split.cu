@@ -232,8 +232,7 @@ cudaError_t launch_split_kernel(const uint32_t *in, const uint32_t *vin, uint32_
                        (!PAIRS || (reinterpret_cast<uintptr_t>(vin) & 15) == 0);
     const size_t smem = static_cast<size_t>(kSplitTile) * (PAIRS ? 2 : 1) * sizeof(uint32_t);
     auto k = k_split<Pred, PAIRS>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(k), smem);
     if (e != cudaSuccess) return e;
     k<<<tiles, kSplitThreads, smem, s>>>(in, vin, out, vout, n, pred, num_true, states, states_clear,
                                          counter, status, abort_flag, spin_limit, stall_tile, vec_ok);

@@ -358,9 +358,10 @@ int gsort_compact_positive_ex(const float *d_in, float *d_out, int64_t n,
 int gsort_radix_num_variants(void);
 const char *gsort_radix_variant_name(int variant);
 
-/* Kernel launches one call makes (for launch accounting):
- * radix: 2 + passes (+1 copy-back when sorting in place with an odd pass
- * count; +1 histogram clear for 64-bit keys, see
+/* Kernel launches one call makes with the default variant (for launch
+ * accounting): radix: 2 for 32-bit keys and n <= 2^18 (one cooperative
+ * kernel runs every pass), else 2 + passes (+1 copy-back when sorting in
+ * place with an odd pass count; +1 histogram clear for 64-bit keys, see
  * gsort_radix_sort_launch_count); compaction: 3; segmented: 1 (0 when
  * there is nothing to do). */
 int gsort_radix_launch_count(int64_t n, int begin_bit, int end_bit, int in_place);

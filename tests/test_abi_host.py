@@ -57,12 +57,14 @@ def test_workspace_sizes(lib):
 
     def up(x):
         return -(-x // 256) * 256
-    for n in (1, 4095, 4096, 4097, 65536, 1 << 24, (1 << 30) - 1):
+    for n in (1, 4095, 4096, 4097, 65536, 1 << 18, (1 << 18) + 1, 1 << 24, (1 << 30) - 1):
         tiles = (n + 4095) // 4096
         state = 2 * up(tiles * 1024)   # two alternating regions of look-back words
         keys = up(n * 4)
-        assert lib.gsort_radix_workspace_bytes(n, 0) == HDR + state + keys
-        assert lib.gsort_radix_workspace_bytes(n, 1) == HDR + state + 2 * keys
+        # up to 2^18 keys: three count buffers of the one-launch sort, a row per 2048 keys
+        small = up(3 * ((n + 2047) // 2048) * 1024) if n <= 1 << 18 else 0
+        assert lib.gsort_radix_workspace_bytes(n, 0) == HDR + state + keys + small
+        assert lib.gsort_radix_workspace_bytes(n, 1) == HDR + state + 2 * keys + small
         ctiles = (n + 8191) // 8192
         assert lib.gsort_compact_workspace_bytes(n) == HDR + up(ctiles * 128)   # a line per tile
     assert lib.gsort_radix_workspace_bytes(-1, 0) == 0
@@ -169,14 +171,17 @@ def test_partition_and_split_sort_argument_errors(lib):
 
 
 def test_launch_count(lib):
-    assert lib.gsort_radix_launch_count(100, 0, 32, 0) == 6
-    assert lib.gsort_radix_launch_count(100, 0, 8, 0) == 3
-    assert lib.gsort_radix_launch_count(100, 0, 24, 1) == 6
+    assert lib.gsort_radix_launch_count(100, 0, 32, 0) == 2          # small input: one cooperative kernel
+    assert lib.gsort_radix_launch_count(1 << 18, 0, 32, 1) == 2
+    assert lib.gsort_radix_launch_count((1 << 18) + 1, 0, 32, 0) == 6
+    assert lib.gsort_radix_launch_count(1 << 20, 0, 8, 0) == 3
+    assert lib.gsort_radix_launch_count(1 << 20, 0, 24, 1) == 6
     assert lib.gsort_radix_launch_count(0, 0, 32, 0) == 0
     assert lib.gsort_radix_launch_count(100, 5, 5, 0) == 0
     assert lib.gsort_radix_sort_launch_count(100, 3, 0, 64, 0) == 11      # 2 + 8 passes + hist clear
     assert lib.gsort_radix_sort_launch_count(100, 5, 0, 56, 1) == 11      # 7 passes, in place: + copy
-    assert lib.gsort_radix_sort_launch_count(100, 2, 0, 32, 0) == 6
+    assert lib.gsort_radix_sort_launch_count(1 << 20, 2, 0, 32, 0) == 6
+    assert lib.gsort_radix_sort_launch_count(100, 2, 0, 32, 0) == 2
 
 
 # Fake device addresses: validation rejects these calls before any CUDA call.

@@ -16,9 +16,12 @@ pytestmark = pytest.mark.gpu
 ETIMEOUT = -6
 
 
+# 2^16 keys take the one-launch small-input kernel (a stalled CTA never reaches
+# the grid barrier); 2^19 keys the per-pass kernels (a stalled tile never
+# publishes, so the look-backs behind it wait)
+@pytest.mark.parametrize("n", [8 * 8192, 64 * 8192])
 @pytest.mark.parametrize("stall", [0, 1, 3])
-def test_radix_wait_gives_up_and_reports(stall):
-    n = 8 * 8192
+def test_radix_wait_gives_up_and_reports(stall, n):
     k = synth.uniform_keys(n, 1)
     with pytest.raises(gsort.GsortError) as e:
         gsort.sort_pairs(dev(k), dev(synth.index_values(n)), spin_limit=2000, stall_tile=stall)
@@ -42,8 +45,8 @@ def test_compaction_wait_gives_up_and_reports(stall):
 
 
 def test_last_tile_stall_is_harmless_to_others():
-    # nothing waits behind the last tile: no timeout, only its own keys are void
-    n = 4 * 8192
+    # a stall id beyond the grid: no timeout
+    n = 64 * 8192
     k = synth.uniform_keys(n, 3)
     ko, _ = gsort.sort_pairs(dev(k), None, spin_limit=2000, stall_tile=10**6)  # no such tile
     assert_bits_equal(host_u32(ko), oracle.radix_sort_keys(k), "stall id beyond the grid")
