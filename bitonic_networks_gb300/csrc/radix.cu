@@ -357,6 +357,10 @@ int launch_radix(const RadixLaunch &L) {
         a.abort_flag = abort_flag;
         a.spin_limit = L.spin_limit;
         a.stall_tile = L.stall_tile;
+        // bulk prefetches need 16-byte aligned sources; about two CTAs per SM are resident
+        const bool src16 = (reinterpret_cast<uintptr_t>(src_k) & 15) == 0 &&
+                           (!pairs || (reinterpret_cast<uintptr_t>(src_v) & 15) == 0);
+        a.prefetch_dist = src16 ? 2u * static_cast<uint32_t>(L.sm_count) : 0u;
         const bool xin = mapped && p == 0;
         const bool xout = mapped && p == passes - 1;
         if (launch(a, pairs, xin, xout, tiles, s) != cudaSuccess) return GSORT_ECUDA;

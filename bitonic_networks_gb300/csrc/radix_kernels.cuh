@@ -64,6 +64,7 @@ struct PassArgs {
     uint32_t *abort_flag;
     uint32_t spin_limit;
     uint32_t stall_tile;
+    uint32_t prefetch_dist;  // a CTA asks L2 for the keys of tile (its tile + this); 0: off
 };
 
 // Launch of one digit pass over `tiles` tiles (one configuration of the kernel).
@@ -542,6 +543,22 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass(const PassArgs 
     __syncthreads();
     const uint32_t tile = s_misc[0];
     if (s_misc[1]) return;   // an earlier wait gave up; the result is void anyway
+    if (tid == 0 && a.prefetch_dist != 0) {
+        // The CTA that claims tile + prefetch_dist (about one CTA lifetime
+        // later) then finds its keys in L2 instead of waiting for HBM.
+        const uint32_t pt = tile + a.prefetch_dist;
+        if (pt < (a.n + TILE - 1) / TILE) {
+            const uint32_t cnt = min(static_cast<uint32_t>(TILE), a.n - pt * TILE);
+            const uint32_t kbytes = (cnt * static_cast<uint32_t>(sizeof(K))) & ~15u;
+            if (kbytes)
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                             ::"l"(static_cast<const K *>(a.src_k) + pt * TILE), "r"(kbytes) : "memory");
+            const uint32_t vbytes = (cnt * 4u) & ~15u;
+            if (PAIRS && vbytes)
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                             ::"l"(a.src_v + pt * TILE), "r"(vbytes) : "memory");
+        }
+    }
     K *s_keys = reinterpret_cast<K *>(smem);
     uint32_t *s_vals = smem + TILE * kKeyWords;
     const K *kin = static_cast<const K *>(a.src_k) + tile * TILE;

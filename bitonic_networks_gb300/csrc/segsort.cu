@@ -515,6 +515,7 @@ int launch_segmented_sort(const SegLaunch &L) {
         a.abort_flag = abort_flag;
         a.spin_limit = L.spin_limit;
         a.stall_tile = kNoStall;
+        a.prefetch_dist = 0;   // tiles map to segments; no prefetch
         const bool xin = mapped && p == 0, xout = mapped && p == 3;
         e = pairs ? SegPassLaunch<true>::launch(a, xin, xout, tiles, counts, hist, pgrid, s)
                   : SegPassLaunch<false>::launch(a, xin, xout, tiles, counts, hist, pgrid, s);
