@@ -309,7 +309,9 @@ def main():
                           "note": "32 B/key = 4 passes x (4 B read + 4 B written); the "
                                   "histogram read (4 B/key) is spent but not counted"},
         "kernels_ms": {"init": sum(init_ms) / len(init_ms), "histogram": sum(hist_ms) / len(hist_ms),
-                       "digit_pass": pass_mean},
+                       "digit_pass": pass_mean,
+                       "digit_pass_each": [sum(pass_ms[s * PASSES + p] for s in range(args.steps)) / args.steps
+                                           for p in range(PASSES)]},
         "gpu_launches": args.steps * lib.gsort_radix_launch_count(n, 0, 32, 0),
         "clocks": clk,
     }

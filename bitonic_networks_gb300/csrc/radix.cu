@@ -361,6 +361,10 @@ int launch_radix(const RadixLaunch &L) {
         const bool src16 = (reinterpret_cast<uintptr_t>(src_k) & 15) == 0 &&
                            (!pairs || (reinterpret_cast<uintptr_t>(src_v) & 15) == 0);
         a.prefetch_dist = src16 ? 2u * static_cast<uint32_t>(L.sm_count) : 0u;
+        // keys only, every bit: equal keys are indistinguishable, so a warp
+        // needs stable ranks only where its keys differ below this digit
+        a.order_free = (!pairs && L.begin_bit == 0 && L.end_bit == static_cast<int>(8 * kb)) ? 1u : 0u;
+        a.free_low = a.shift >= 64 ? ~0ull : ((1ull << a.shift) - 1ull);
         const bool xin = mapped && p == 0;
         const bool xout = mapped && p == passes - 1;
         if (launch(a, pairs, xin, xout, tiles, s) != cudaSuccess) return GSORT_ECUDA;

@@ -65,6 +65,12 @@ struct PassArgs {
     uint32_t spin_limit;
     uint32_t stall_tile;
     uint32_t prefetch_dist;  // a CTA asks L2 for the keys of tile (its tile + this); 0: off
+    // Keys-only sort over every bit of the key: a warp whose keys all agree
+    // in the bits `free_low` (the bits below this pass's digit, by which the
+    // input is already sorted) may rank them in any order, since such keys
+    // with one digit agree in every bit sorted so far.
+    uint32_t order_free = 0;
+    uint64_t free_low = 0;
 };
 
 // Launch of one digit pass over `tiles` tiles (one configuration of the kernel).
@@ -481,6 +487,24 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, cons
         s_goff[tid] = td.out_base + bin_excl + excl - tile_excl;
     }
 
+    // ---- order-free warps: the warp's keys are sorted by the bits below this
+    // digit (the earlier passes' order), so if its first and last keys agree
+    // there, all of them do, and keys of one digit are interchangeable: each
+    // takes the next free slot of its digit (one shared atomic, no ballots)
+    bool order_free = false;
+    if constexpr (!PAIRS && FULL) {
+        if (a.order_free) {
+            const K first = __shfl_sync(kFullMask, key[0], 0);
+            const K last = __shfl_sync(kFullMask, key[IPT - 1], 31);
+            order_free = ((first ^ last) & static_cast<K>(a.free_low)) == 0;
+        }
+    }
+    if (order_free) {
+        uint32_t *wc = s_cnt + warp * kRow;
+#pragma unroll
+        for (int k = 0; k < IPT; ++k)
+            s_keys[atomicAdd(&wc[digit_at<BYTE>(key[k], a.shift, a.mask)], 1u)] = key[k];
+    } else
     // ---- warp multisplit: stable slot of each key in the tile-sorted order
     {
         uint32_t *wc = s_cnt + warp * kRow;

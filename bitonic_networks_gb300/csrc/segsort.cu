@@ -516,6 +516,9 @@ int launch_segmented_sort(const SegLaunch &L) {
         a.spin_limit = L.spin_limit;
         a.stall_tile = kNoStall;
         a.prefetch_dist = 0;   // tiles map to segments; no prefetch
+        // keys only: equal keys are indistinguishable (tiles never cross a segment)
+        a.order_free = pairs ? 0u : 1u;
+        a.free_low = (1ull << a.shift) - 1ull;
         const bool xin = mapped && p == 0, xout = mapped && p == 3;
         e = pairs ? SegPassLaunch<true>::launch(a, xin, xout, tiles, counts, hist, pgrid, s)
                   : SegPassLaunch<false>::launch(a, xin, xout, tiles, counts, hist, pgrid, s);
