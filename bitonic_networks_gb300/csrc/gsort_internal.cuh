@@ -19,6 +19,7 @@ constexpr size_t kHdrCounters = 128;  // u32 tile counters, one per 128-byte lin
 constexpr int kNumCounters = 8;
 constexpr size_t kHdrKept = kHdrCounters + 128 * kNumCounters;  // u64 kept count (compaction)
 constexpr size_t kHdrHist = 2048;     // u32[4][256] digit histograms (radix, 32-bit keys)
+constexpr size_t kHdrCursor = kHdrHist + 4096;   // u32[256] bin cursors of an order-free first pass (radix)
 constexpr size_t kHdrBytes = 8192;    // header size, keeps what follows 256-byte aligned
 constexpr size_t kWsAlign = 256;
 

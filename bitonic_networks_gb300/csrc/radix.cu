@@ -173,20 +173,27 @@ struct PersistentConfig {
 };
 
 
+// `free_launch`: the first pass of a keys-only sort over every bit, where
+// every warp is order-free (same tile; null: the variant's own kernel, in its
+// bin-cursor mode).
 struct Variant {
     const char *name;
     uint32_t tile;
     PassLauncher launch;
+    PassLauncher free_launch;
 };
 
 const Variant kVariants[] = {
     {"one tile per CTA, 16 warps x 16 items", PassConfig<uint32_t, 16, 16, 2, kMatchTable>::kTile,
-     &PassConfig<uint32_t, 16, 16, 2, kMatchTable>::launch},
+     &PassConfig<uint32_t, 16, 16, 2, kMatchTable>::launch, &FreePassConfig<uint32_t, 16, 16, 3>::launch},
     {"persistent, 16 warps x 16 items, TMA prefetch", PersistentConfig<16, 16, kMatchTable>::kTile,
-     &PersistentConfig<16, 16, kMatchTable>::launch},
+     &PersistentConfig<16, 16, kMatchTable>::launch, nullptr},
     {"one tile per CTA, 8 warps x 16 items", PassConfig<uint32_t, 8, 16, 3, kMatchTable>::kTile,
-     &PassConfig<uint32_t, 8, 16, 3, kMatchTable>::launch},
+     &PassConfig<uint32_t, 8, 16, 3, kMatchTable>::launch, &FreePassConfig<uint32_t, 8, 16, 4>::launch},
 };
+static_assert(FreePassConfig<uint32_t, 16, 16, 3>::kTile == PassConfig<uint32_t, 16, 16, 2, kMatchTable>::kTile &&
+                  FreePassConfig<uint32_t, 8, 16, 4>::kTile == PassConfig<uint32_t, 8, 16, 3, kMatchTable>::kTile,
+              "an order-free first pass keeps its variant's tile");
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 
 void record(cudaEvent_t *ev, int num, int idx, cudaStream_t s) {
@@ -267,6 +274,7 @@ int launch_radix(const RadixLaunch &L) {
     // 64-bit keys have one configuration; 32-bit keys take the chosen variant
     const uint32_t tile = kb == 8 ? pass_tile_u64() : kVariants[L.variant].tile;
     const PassLauncher launch = kb == 8 ? &launch_pass_u64 : kVariants[L.variant].launch;
+    const PassLauncher free_launch = kb == 8 ? &launch_pass_u64_free : kVariants[L.variant].free_launch;
     const uint32_t tiles = (L.n + tile - 1) / tile;
     cudaStream_t s = L.stream;
 
@@ -365,9 +373,14 @@ int launch_radix(const RadixLaunch &L) {
         // needs stable ranks only where its keys differ below this digit
         a.order_free = (!pairs && L.begin_bit == 0 && L.end_bit == static_cast<int>(8 * kb)) ? 1u : 0u;
         a.free_low = a.shift >= 64 ? ~0ull : ((1ull << a.shift) - 1ull);
+        // runs of equal low bits hold about n / 2^shift keys of uniform input;
+        // below half a warp's keys (512), two-value warps are rare
+        a.two_runs_ok = (a.shift < 32 && (static_cast<uint64_t>(L.n) >> a.shift) >= 256) ? 1u : 0u;
+        a.cursor = (a.order_free && p == 0) ? reinterpret_cast<uint32_t *>(L.ws + kHdrCursor) : nullptr;
         const bool xin = mapped && p == 0;
         const bool xout = mapped && p == passes - 1;
-        if (launch(a, pairs, xin, xout, tiles, s) != cudaSuccess) return GSORT_ECUDA;
+        const PassLauncher use = a.cursor != nullptr && free_launch != nullptr ? free_launch : launch;
+        if (use(a, pairs, xin, xout, tiles, s) != cudaSuccess) return GSORT_ECUDA;
         record(L.events, L.num_events, 3 + p, s);
         src_k = dst_k;
         src_v = dst_v;

@@ -71,6 +71,14 @@ struct PassArgs {
     // with one digit agree in every bit sorted so far.
     uint32_t order_free = 0;
     uint64_t free_low = 0;
+    // Non-zero: a warp whose keys take two values in `free_low` may rank in
+    // two order-free rounds (worth testing only where runs are long).
+    uint32_t two_runs_ok = 0;
+    // Non-null (first pass of such a sort, where every warp is order-free):
+    // any tile may take any place inside a digit's bin, so a tile reserves
+    // its places with one atomic add per digit on these 256 bin cursors
+    // (zeroed) instead of looking back, and takes its tile by block index.
+    uint32_t *cursor = nullptr;
 };
 
 // Launch of one digit pass over `tiles` tiles (one configuration of the kernel).
@@ -80,6 +88,8 @@ using PassLauncher = cudaError_t (*)(const PassArgs &, bool pairs, bool xin, boo
 // 64-bit keys (radix64.cu): the digit pass, its tile size, and the histogram.
 cudaError_t launch_pass_u64(const PassArgs &a, bool pairs, bool xin, bool xout, uint32_t tiles,
                             cudaStream_t s);
+cudaError_t launch_pass_u64_free(const PassArgs &a, bool pairs, bool xin, bool xout, uint32_t tiles,
+                                 cudaStream_t s);
 uint32_t pass_tile_u64();
 cudaError_t launch_hist_u64(const uint64_t *keys, uint32_t n, bool xf, uint64_t fmask, uint64_t flip,
                             int begin_bit, int passes, uint32_t last_mask, uint32_t *hist,
@@ -392,7 +402,7 @@ struct NoHook {
 };
 
 template <class K, int WARPS, int IPT, int MATCH, int LW, bool BYTE, bool PAIRS, bool XIN, bool XOUT,
-          bool FULL, class Hook = NoHook>
+          bool FULL, bool FREE_ONLY = false, class Hook = NoHook>
 __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, const TileDesc &td,
                                           const K *kin, const uint32_t *vin,
                                           K *s_keys, uint32_t *s_vals,
@@ -444,7 +454,7 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, cons
             s_cnt[w * kRow + tid] = cnt;   // exclusive over warps
             cnt += cw;
         }
-        if (tile != a.stall_tile)
+        if (!FREE_ONLY && tile != a.stall_tile && a.cursor == nullptr)
             st_relaxed(a.look + tile * 256 + tid, (tile == td.first ? kFlagPrefix : kFlagAgg) | cnt);
         const uint32_t bin = td.hist[tid];
         const uint32_t ic = warp_inclusive_scan(cnt, lane);
@@ -475,7 +485,9 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, cons
     if (tid < 256) {
         uint32_t excl = 0;
         bool ok = true;
-        if (tile > td.first && tile != a.stall_tile) {
+        if (FREE_ONLY || a.cursor != nullptr) {
+            if (cnt != 0 && tile != a.stall_tile) excl = atomicAdd(a.cursor + tid, cnt);
+        } else if (tile > td.first && tile != a.stall_tile) {
             ok = look_back<LW>(a, td, tid, excl);
             if (ok) st_relaxed(a.look + tile * 256 + tid, kFlagPrefix | (excl + cnt));
         }
@@ -491,20 +503,49 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, cons
     // digit (the earlier passes' order), so if its first and last keys agree
     // there, all of them do, and keys of one digit are interchangeable: each
     // takes the next free slot of its digit (one shared atomic, no ballots)
-    bool order_free = false;
-    if constexpr (!PAIRS && FULL) {
+    // A warp whose keys take exactly two values in those bits (a run boundary
+    // inside the warp) ranks in two rounds: every key of the first value,
+    // then, after a warp barrier, every key of the second, so that the first
+    // value's keys of each digit take the lower slots.
+    bool order_free = FREE_ONLY, two_runs = false;
+    K low_first = 0;
+    if constexpr (!PAIRS && FULL && !FREE_ONLY) {
         if (a.order_free) {
-            const K first = __shfl_sync(kFullMask, key[0], 0);
-            const K last = __shfl_sync(kFullMask, key[IPT - 1], 31);
-            order_free = ((first ^ last) & static_cast<K>(a.free_low)) == 0;
+            const K fl = static_cast<K>(a.free_low);
+            low_first = __shfl_sync(kFullMask, key[0], 0) & fl;
+            const K low_last = __shfl_sync(kFullMask, key[IPT - 1], 31) & fl;
+            order_free = low_first == low_last;
+            if (!order_free && a.two_runs_ok) {
+                bool two = true;
+#pragma unroll
+                for (int k = 0; k < IPT; ++k) {
+                    const K lo = key[k] & fl;
+                    two &= lo == low_first || lo == low_last;
+                }
+                order_free = two_runs = __all_sync(kFullMask, two);
+            }
         }
     }
     if (order_free) {
         uint32_t *wc = s_cnt + warp * kRow;
+        if (!two_runs) {
 #pragma unroll
-        for (int k = 0; k < IPT; ++k)
-            s_keys[atomicAdd(&wc[digit_at<BYTE>(key[k], a.shift, a.mask)], 1u)] = key[k];
-    } else
+            for (int k = 0; k < IPT; ++k)
+                if (FULL || item0 + k * 32 < tile_n)
+                    s_keys[atomicAdd(&wc[digit_at<BYTE>(key[k], a.shift, a.mask)], 1u)] = key[k];
+        } else {
+            const K fl = static_cast<K>(a.free_low);
+#pragma unroll
+            for (int k = 0; k < IPT; ++k)
+                if ((key[k] & fl) == low_first)
+                    s_keys[atomicAdd(&wc[digit_at<BYTE>(key[k], a.shift, a.mask)], 1u)] = key[k];
+            __syncwarp();   // the first run's slots are taken before the second run's
+#pragma unroll
+            for (int k = 0; k < IPT; ++k)
+                if ((key[k] & fl) != low_first)
+                    s_keys[atomicAdd(&wc[digit_at<BYTE>(key[k], a.shift, a.mask)], 1u)] = key[k];
+        }
+    } else if constexpr (!FREE_ONLY)
     // ---- warp multisplit: stable slot of each key in the tile-sorted order
     {
         uint32_t *wc = s_cnt + warp * kRow;
@@ -550,14 +591,17 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, cons
 }
 
 template <class K, int WARPS, int IPT, int MINB, int MATCH, int LW, bool BYTE, bool PAIRS, bool XIN,
-          bool XOUT>
+          bool XOUT, bool FREE_ONLY = false>
 __global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass(const PassArgs a) {
+    static_assert(!(FREE_ONLY && PAIRS), "order-free passes move keys only");
     constexpr int TILE = WARPS * 32 * IPT;
     extern __shared__ __align__(128) uint32_t smem[];
     uint32_t *s_misc = smem + pass_smem_words<K, WARPS, IPT, PAIRS>() - 32;
     const uint32_t tid = threadIdx.x;
     if (tid == 0) {
-        s_misc[0] = atomicAdd(a.tile_counter, 1u);   // tiles in start order: look-back always progresses
+        // tiles in start order, so that a look-back always progresses; with
+        // bin cursors no tile waits for another and the block index serves
+        s_misc[0] = (FREE_ONLY || a.cursor != nullptr) ? blockIdx.x : atomicAdd(a.tile_counter, 1u);
         s_misc[1] = ld_relaxed(a.abort_flag);
         s_misc[2] = 0;
     }
@@ -589,9 +633,11 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass(const PassArgs 
     const uint32_t *vin = PAIRS ? a.src_v + tile * TILE : nullptr;
     const TileDesc td{tile, 0u, min(static_cast<uint32_t>(TILE), a.n - tile * TILE), a.hist, 0u, a.n};
     if (td.n == static_cast<uint32_t>(TILE))
-        pass_tile<K, WARPS, IPT, MATCH, LW, BYTE, PAIRS, XIN, XOUT, true>(a, s_cnt, td, kin, vin, s_keys, s_vals);
+        pass_tile<K, WARPS, IPT, MATCH, LW, BYTE, PAIRS, XIN, XOUT, true, FREE_ONLY>(a, s_cnt, td, kin, vin,
+                                                                                  s_keys, s_vals);
     else
-        pass_tile<K, WARPS, IPT, MATCH, LW, BYTE, PAIRS, XIN, XOUT, false>(a, s_cnt, td, kin, vin, s_keys, s_vals);
+        pass_tile<K, WARPS, IPT, MATCH, LW, BYTE, PAIRS, XIN, XOUT, false, FREE_ONLY>(a, s_cnt, td, kin, vin,
+                                                                                   s_keys, s_vals);
 }
 
 // One-tile-per-CTA launch configuration of the digit pass.
@@ -630,6 +676,40 @@ struct PassConfig {
         const bool byte = (a.shift % 8) == 0 && a.mask == 0xFFu;
         return byte ? launch_b<true>(a, pairs, xin, xout, tiles, s)
                     : launch_b<false>(a, pairs, xin, xout, tiles, s);
+    }
+};
+
+// Launch configuration of the first pass of a keys-only sort over every bit
+// (bin cursors, every warp order-free): no multisplit and no look-back are
+// compiled in, so the kernel needs fewer registers and more CTAs share an SM.
+// Its tile must not exceed the next pass's, so that clearing row `tile` of the
+// next pass's look-back words covers every row that pass uses.
+template <class K, int WARPS, int IPT, int MINB>
+struct FreePassConfig {
+    static constexpr uint32_t kTile = WARPS * 32 * IPT;
+
+    template <bool B, bool XI, bool XO>
+    static cudaError_t launch_one(const PassArgs &a, uint32_t tiles, cudaStream_t s) {
+        auto k = k_digit_pass<K, WARPS, IPT, MINB, kMatchTable, 8, B, false, XI, XO, true>;
+        const size_t smem = pass_smem_words<K, WARPS, IPT, false>() * sizeof(uint32_t);
+        cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(k), smem);
+        if (e != cudaSuccess) return e;
+        k<<<tiles, WARPS * 32, smem, s>>>(a);
+        return cudaGetLastError();
+    }
+
+    template <bool B>
+    static cudaError_t launch_b(const PassArgs &a, bool xin, bool xout, uint32_t tiles, cudaStream_t s) {
+        if (xin) return xout ? launch_one<B, true, true>(a, tiles, s) : launch_one<B, true, false>(a, tiles, s);
+        return xout ? launch_one<B, false, true>(a, tiles, s) : launch_one<B, false, false>(a, tiles, s);
+    }
+
+    // `tiles` counts tiles of kTile keys.
+    static cudaError_t launch(const PassArgs &a, bool pairs, bool xin, bool xout, uint32_t tiles,
+                              cudaStream_t s) {
+        if (pairs || a.cursor == nullptr) return cudaErrorInvalidValue;
+        const bool byte = (a.shift % 8) == 0 && a.mask == 0xFFu;
+        return byte ? launch_b<true>(a, xin, xout, tiles, s) : launch_b<false>(a, xin, xout, tiles, s);
     }
 };
 

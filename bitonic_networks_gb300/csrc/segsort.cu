@@ -519,6 +519,7 @@ int launch_segmented_sort(const SegLaunch &L) {
         // keys only: equal keys are indistinguishable (tiles never cross a segment)
         a.order_free = pairs ? 0u : 1u;
         a.free_low = (1ull << a.shift) - 1ull;
+        a.two_runs_ok = p <= 1 ? 1u : 0u;   // later passes see short runs in any segment
         const bool xin = mapped && p == 0, xout = mapped && p == 3;
         e = pairs ? SegPassLaunch<true>::launch(a, xin, xout, tiles, counts, hist, pgrid, s)
                   : SegPassLaunch<false>::launch(a, xin, xout, tiles, counts, hist, pgrid, s);
