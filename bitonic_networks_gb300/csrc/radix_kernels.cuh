@@ -328,6 +328,20 @@ __device__ __forceinline__ uint32_t digit_peers(uint32_t d, const LaneConsts &c)
     }
 }
 
+// Next free slot of digit d for this lane's key, from counter table `tab`
+// (order among the warp's keys of one digit is free).  `one_digit`: every lane
+// of the warp holds digit d (runs of equal keys); one lane then reserves all
+// 32 slots, because same-address shared atomics that return a value
+// serialise across the lanes (reductions and distinct addresses do not).
+__device__ __forceinline__ uint32_t take_slot(uint32_t *tab, uint32_t d, uint32_t lane, bool one_digit) {
+    if (one_digit) {
+        uint32_t base = 0;
+        if (lane == 0) base = atomicAdd(&tab[d], 32u);
+        return __shfl_sync(kFullMask, base, 0) + lane;
+    }
+    return atomicAdd(&tab[d], 1u);
+}
+
 constexpr int kRow = 256;   // per-warp digit counters
 
 template <class K, int WARPS, int IPT, bool PAIRS>
@@ -402,7 +416,7 @@ struct NoHook {
 };
 
 template <class K, int WARPS, int IPT, int MATCH, int LW, bool BYTE, bool PAIRS, bool XIN, bool XOUT,
-          bool FULL, bool FREE_ONLY = false, class Hook = NoHook>
+          bool FULL, class Hook = NoHook>
 __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, const TileDesc &td,
                                           const K *kin, const uint32_t *vin,
                                           K *s_keys, uint32_t *s_vals,
@@ -436,12 +450,22 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, cons
         }
     }
 
-    // ---- early counts: this warp's keys per digit (order does not matter here)
+    // ---- early counts: this warp's keys per digit (order does not matter
+    // here); keys-only sorts also note whether all the warp's keys share a digit
+    bool one_digit = false;
     {
         uint32_t *wc = s_cnt + warp * kRow;
+        const uint32_t d0 = __shfl_sync(kFullMask, digit_at<BYTE>(key[0], a.shift, a.mask), 0);
+        bool same = true;
 #pragma unroll
-        for (int k = 0; k < IPT; ++k)
-            if (FULL || item0 + k * 32 < tile_n) atomicAdd(&wc[digit_at<BYTE>(key[k], a.shift, a.mask)], 1u);
+        for (int k = 0; k < IPT; ++k) {
+            if (FULL || item0 + k * 32 < tile_n) {
+                const uint32_t d = digit_at<BYTE>(key[k], a.shift, a.mask);
+                atomicAdd(&wc[d], 1u);
+                same &= d == d0;
+            }
+        }
+        if constexpr (!PAIRS && FULL) one_digit = __all_sync(kFullMask, same);
     }
     __syncthreads();
 
@@ -454,7 +478,7 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, cons
             s_cnt[w * kRow + tid] = cnt;   // exclusive over warps
             cnt += cw;
         }
-        if (!FREE_ONLY && tile != a.stall_tile && a.cursor == nullptr)
+        if (tile != a.stall_tile && a.cursor == nullptr)
             st_relaxed(a.look + tile * 256 + tid, (tile == td.first ? kFlagPrefix : kFlagAgg) | cnt);
         const uint32_t bin = td.hist[tid];
         const uint32_t ic = warp_inclusive_scan(cnt, lane);
@@ -485,7 +509,7 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, cons
     if (tid < 256) {
         uint32_t excl = 0;
         bool ok = true;
-        if (FREE_ONLY || a.cursor != nullptr) {
+        if (a.cursor != nullptr) {
             if (cnt != 0 && tile != a.stall_tile) excl = atomicAdd(a.cursor + tid, cnt);
         } else if (tile > td.first && tile != a.stall_tile) {
             ok = look_back<LW>(a, td, tid, excl);
@@ -507,9 +531,9 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, cons
     // inside the warp) ranks in two rounds: every key of the first value,
     // then, after a warp barrier, every key of the second, so that the first
     // value's keys of each digit take the lower slots.
-    bool order_free = FREE_ONLY, two_runs = false;
+    bool order_free = false, two_runs = false;
     K low_first = 0;
-    if constexpr (!PAIRS && FULL && !FREE_ONLY) {
+    if constexpr (!PAIRS && FULL) {
         if (a.order_free) {
             const K fl = static_cast<K>(a.free_low);
             low_first = __shfl_sync(kFullMask, key[0], 0) & fl;
@@ -530,9 +554,8 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, cons
         uint32_t *wc = s_cnt + warp * kRow;
         if (!two_runs) {
 #pragma unroll
-            for (int k = 0; k < IPT; ++k)
-                if (FULL || item0 + k * 32 < tile_n)
-                    s_keys[atomicAdd(&wc[digit_at<BYTE>(key[k], a.shift, a.mask)], 1u)] = key[k];
+            for (int k = 0; k < IPT; ++k)   // order-free warps come from full tiles only
+                s_keys[take_slot(wc, digit_at<BYTE>(key[k], a.shift, a.mask), lane, one_digit)] = key[k];
         } else {
             const K fl = static_cast<K>(a.free_low);
 #pragma unroll
@@ -545,7 +568,7 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, cons
                 if ((key[k] & fl) != low_first)
                     s_keys[atomicAdd(&wc[digit_at<BYTE>(key[k], a.shift, a.mask)], 1u)] = key[k];
         }
-    } else if constexpr (!FREE_ONLY)
+    } else
     // ---- warp multisplit: stable slot of each key in the tile-sorted order
     {
         uint32_t *wc = s_cnt + warp * kRow;
@@ -591,9 +614,8 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, cons
 }
 
 template <class K, int WARPS, int IPT, int MINB, int MATCH, int LW, bool BYTE, bool PAIRS, bool XIN,
-          bool XOUT, bool FREE_ONLY = false>
+          bool XOUT>
 __global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass(const PassArgs a) {
-    static_assert(!(FREE_ONLY && PAIRS), "order-free passes move keys only");
     constexpr int TILE = WARPS * 32 * IPT;
     extern __shared__ __align__(128) uint32_t smem[];
     uint32_t *s_misc = smem + pass_smem_words<K, WARPS, IPT, PAIRS>() - 32;
@@ -601,7 +623,7 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass(const PassArgs 
     if (tid == 0) {
         // tiles in start order, so that a look-back always progresses; with
         // bin cursors no tile waits for another and the block index serves
-        s_misc[0] = (FREE_ONLY || a.cursor != nullptr) ? blockIdx.x : atomicAdd(a.tile_counter, 1u);
+        s_misc[0] = a.cursor != nullptr ? blockIdx.x : atomicAdd(a.tile_counter, 1u);
         s_misc[1] = ld_relaxed(a.abort_flag);
         s_misc[2] = 0;
     }
@@ -633,11 +655,9 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass(const PassArgs 
     const uint32_t *vin = PAIRS ? a.src_v + tile * TILE : nullptr;
     const TileDesc td{tile, 0u, min(static_cast<uint32_t>(TILE), a.n - tile * TILE), a.hist, 0u, a.n};
     if (td.n == static_cast<uint32_t>(TILE))
-        pass_tile<K, WARPS, IPT, MATCH, LW, BYTE, PAIRS, XIN, XOUT, true, FREE_ONLY>(a, s_cnt, td, kin, vin,
-                                                                                  s_keys, s_vals);
+        pass_tile<K, WARPS, IPT, MATCH, LW, BYTE, PAIRS, XIN, XOUT, true>(a, s_cnt, td, kin, vin, s_keys, s_vals);
     else
-        pass_tile<K, WARPS, IPT, MATCH, LW, BYTE, PAIRS, XIN, XOUT, false, FREE_ONLY>(a, s_cnt, td, kin, vin,
-                                                                                   s_keys, s_vals);
+        pass_tile<K, WARPS, IPT, MATCH, LW, BYTE, PAIRS, XIN, XOUT, false>(a, s_cnt, td, kin, vin, s_keys, s_vals);
 }
 
 // One-tile-per-CTA launch configuration of the digit pass.
@@ -679,19 +699,144 @@ struct PassConfig {
     }
 };
 
-// Launch configuration of the first pass of a keys-only sort over every bit
-// (bin cursors, every warp order-free): no multisplit and no look-back are
-// compiled in, so the kernel needs fewer registers and more CTAs share an SM.
-// Its tile must not exceed the next pass's, so that clearing row `tile` of the
-// next pass's look-back words covers every row that pass uses.
+// ------------------------------------------- order-free first digit pass
+// First pass of a keys-only sort over every bit of the key.  Equal keys are
+// indistinguishable and no earlier pass fixed an order, so the keys of one
+// digit may land in any order, within a tile and across tiles:
+//   - one shared counter per digit for the whole tile; the atomic add that
+//     counts a key also returns its rank among the tile's keys of its digit
+//     (no per-warp tables, no warp-order scans, no multisplit);
+//   - the tile reserves its places inside each digit's bin with one atomic
+//     add per digit on 256 bin cursors (no look-back, no wait on any other
+//     tile), and takes its tile by block index;
+//   - the tile is reordered in shared memory and written as per-digit runs,
+//     as in the stable pass.
+// Shared memory: keys of the tile, 256 counts/tile offsets, 256 global
+// offsets, 32 misc words.
+template <class K, int WARPS, int IPT>
+__host__ __device__ constexpr size_t free_pass_smem_words() {
+    return static_cast<size_t>(WARPS * 32 * IPT) * (sizeof(K) / 4) + 256 + 256 + 32;
+}
+
+template <class K, int WARPS, int IPT, int MINB, bool BYTE, bool XIN, bool XOUT>
+__global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass_free(const PassArgs a) {
+    static_assert(WARPS * 32 >= 256, "one thread per digit");
+    static_assert(IPT % 2 == 0, "ranks are packed two per register");
+    constexpr int T = WARPS * 32;
+    constexpr int TILE = T * IPT;
+    extern __shared__ __align__(128) uint32_t smem[];
+    K *s_keys = reinterpret_cast<K *>(smem);
+    uint32_t *s_cnt = smem + TILE * (sizeof(K) / 4);   // [256] counts, then tile offsets
+    uint32_t *s_goff = s_cnt + 256;                    // [256] global index - tile slot
+    uint32_t *s_misc = s_goff + 256;                   // [32]
+    const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t tile = blockIdx.x;
+    const uint32_t tile_n = min(static_cast<uint32_t>(TILE), a.n - tile * TILE);
+    const K *kin = static_cast<const K *>(a.src_k) + static_cast<size_t>(tile) * TILE;
+
+    // keys first (their latency overlaps the table set-up)
+    K key[IPT];
+#pragma unroll
+    for (int k = 0; k < IPT; ++k) {
+        const uint32_t i = k * T + tid;
+        key[k] = i < tile_n ? kin[i] : K(0);
+        if (XIN) key[k] = order_in<K>(key[k], static_cast<K>(a.fmask), static_cast<K>(a.flip));
+    }
+    if (tid < 256) s_cnt[tid] = 0;
+    if (tid == 0) s_misc[0] = ld_relaxed(a.abort_flag);
+    __syncthreads();
+    if (s_misc[0]) return;   // an earlier wait gave up; the result is void anyway
+
+    // count and rank in one shared atomic per key (one per item when all the
+    // warp's keys share a digit: presorted or constant input)
+    bool one_digit = false;
+    if (tile_n == static_cast<uint32_t>(TILE)) {   // tile-uniform
+        const uint32_t d0 = __shfl_sync(kFullMask, digit_at<BYTE>(key[0], a.shift, a.mask), 0);
+        bool same = true;
+#pragma unroll
+        for (int k = 0; k < IPT; ++k) same &= digit_at<BYTE>(key[k], a.shift, a.mask) == d0;
+        one_digit = __all_sync(kFullMask, same);
+    }
+    uint32_t rk[IPT / 2];
+#pragma unroll
+    for (int k = 0; k < IPT; k += 2) {
+        uint32_t r0 = 0, r1 = 0;
+        if (one_digit) {
+            r0 = take_slot(s_cnt, digit_at<BYTE>(key[k], a.shift, a.mask), lane, true);
+            r1 = take_slot(s_cnt, digit_at<BYTE>(key[k + 1], a.shift, a.mask), lane, true);
+        } else {
+            if (k * T + tid < tile_n) r0 = atomicAdd(&s_cnt[digit_at<BYTE>(key[k], a.shift, a.mask)], 1u);
+            if ((k + 1) * T + tid < tile_n)
+                r1 = atomicAdd(&s_cnt[digit_at<BYTE>(key[k + 1], a.shift, a.mask)], 1u);
+        }
+        rk[k / 2] = r0 | (r1 << 16);
+    }
+    __syncthreads();
+
+    // scans over the 256 digits: tile offsets and bin starts
+    uint32_t cnt = 0, tile_excl = 0, bin_excl = 0;
+    if (tid < 256) {
+        cnt = s_cnt[tid];
+        const uint32_t bin = a.hist[tid];
+        const uint32_t ic = warp_inclusive_scan(cnt, lane);
+        const uint32_t ib = warp_inclusive_scan(bin, lane);
+        if (lane == 31) {
+            s_misc[4 + warp] = ic;
+            s_misc[12 + warp] = ib;
+        }
+        tile_excl = ic - cnt;
+        bin_excl = ib - bin;
+    }
+    __syncthreads();
+    if (tid < 256) {
+        for (uint32_t w = 0; w < warp; ++w) {
+            tile_excl += s_misc[4 + w];
+            bin_excl += s_misc[12 + w];
+        }
+        s_cnt[tid] = tile_excl;
+    }
+    __syncthreads();
+
+    // reserve the tile's places in the bins (in flight during the reorder)
+    uint32_t excl = 0;
+    if (tid < 256 && cnt != 0 && tile != a.stall_tile) excl = atomicAdd(a.cursor + tid, cnt);
+    if (a.look_clear != nullptr)
+        for (uint32_t i = tid; i < 256; i += T) a.look_clear[tile * 256 + i] = 0;
+#pragma unroll
+    for (int k = 0; k < IPT; ++k) {
+        if (k * T + tid < tile_n) {
+            const uint32_t r = (rk[k / 2] >> ((k & 1) * 16)) & 0xFFFFu;
+            s_keys[s_cnt[digit_at<BYTE>(key[k], a.shift, a.mask)] + r] = key[k];
+        }
+    }
+    if (tid < 256) s_goff[tid] = bin_excl + excl - tile_excl;
+    __syncthreads();
+    if (tile == a.stall_tile) return;
+
+    // contiguous runs per digit out to global memory
+    K *dst_k = static_cast<K *>(a.dst_k);
+#pragma unroll
+    for (int k = 0; k < IPT; ++k) {
+        const uint32_t i = k * T + tid;
+        if (i < tile_n) {
+            const K kk = s_keys[i];
+            const uint32_t g = s_goff[digit_at<BYTE>(kk, a.shift, a.mask)] + i;
+            if (g < a.n) dst_k[g] = XOUT ? order_out<K>(kk, static_cast<K>(a.fmask), static_cast<K>(a.flip)) : kk;
+        }
+    }
+}
+
+// Launch configuration of the order-free first pass (k_digit_pass_free).
+// Its tile must not exceed the next pass's, so that clearing row `tile` of
+// the next pass's look-back words covers every row that pass uses.
 template <class K, int WARPS, int IPT, int MINB>
 struct FreePassConfig {
     static constexpr uint32_t kTile = WARPS * 32 * IPT;
 
     template <bool B, bool XI, bool XO>
     static cudaError_t launch_one(const PassArgs &a, uint32_t tiles, cudaStream_t s) {
-        auto k = k_digit_pass<K, WARPS, IPT, MINB, kMatchTable, 8, B, false, XI, XO, true>;
-        const size_t smem = pass_smem_words<K, WARPS, IPT, false>() * sizeof(uint32_t);
+        auto k = k_digit_pass_free<K, WARPS, IPT, MINB, B, XI, XO>;
+        const size_t smem = free_pass_smem_words<K, WARPS, IPT>() * sizeof(uint32_t);
         cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(k), smem);
         if (e != cudaSuccess) return e;
         k<<<tiles, WARPS * 32, smem, s>>>(a);
