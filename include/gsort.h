@@ -88,6 +88,14 @@ int gsort_version(void);
  * where the middle term comes from a decoupled look-back over per-(tile,
  * digit) counts.  Equal keys keep their input order; values move with keys.
  *
+ * Keys only, sorted by every bit of the key: equal keys are identical, so a
+ * pass needs the input order only between keys that differ in the bits
+ * below its digit.  There the first pass places keys in any order within
+ * their bin (atomic bin cursors instead of the look-back), and a warp whose
+ * keys agree below the digit ranks them by shared atomics instead of the
+ * multisplit.  The output is the same (a sorted key sequence is unique);
+ * the intermediate order may differ from run to run.
+ *
  * Float keys (GSORT_KEY_F32): the bit pattern is mapped to an unsigned
  * integer that orders every non-NaN value as IEEE totalOrder (-inf < ... <
  * -0 < +0 < ... < +inf); the output holds the original bit patterns.
