@@ -173,6 +173,21 @@ struct PersistentConfig {
 };
 
 
+// Keys and pairs in one variant with different occupancy: keys-only passes
+// fit 40 registers without spilling, so three CTAs share an SM; pairs hold
+// twice the registers per item and keep two.
+template <class KeysCfg, class PairsCfg>
+struct KeysPairsConfig {
+    static_assert(KeysCfg::kTile == PairsCfg::kTile, "one tile size per variant");
+    static constexpr uint32_t kTile = KeysCfg::kTile;
+    static cudaError_t launch(const PassArgs &a, bool pairs, bool xin, bool xout, uint32_t tiles,
+                              cudaStream_t s) {
+        return pairs ? PairsCfg::launch(a, pairs, xin, xout, tiles, s)
+                     : KeysCfg::launch_keys(a, pairs, xin, xout, tiles, s);
+    }
+};
+using Variant0 = KeysPairsConfig<PassConfig<uint32_t, 16, 16, 3, kMatchTable>, PassConfig<uint32_t, 16, 16, 2, kMatchTable>>;
+
 // `free_launch`: the first pass of a keys-only sort over every bit, where
 // every warp is order-free (same tile; null: the variant's own kernel, in its
 // bin-cursor mode).
@@ -184,14 +199,14 @@ struct Variant {
 };
 
 const Variant kVariants[] = {
-    {"one tile per CTA, 16 warps x 16 items", PassConfig<uint32_t, 16, 16, 2, kMatchTable>::kTile,
-     &PassConfig<uint32_t, 16, 16, 2, kMatchTable>::launch, &FreePassConfig<uint32_t, 16, 16, 3>::launch},
+    {"one tile per CTA, 16 warps x 16 items", Variant0::kTile, &Variant0::launch,
+     &FreePassConfig<uint32_t, 16, 16, 3>::launch},
     {"persistent, 16 warps x 16 items, TMA prefetch", PersistentConfig<16, 16, kMatchTable>::kTile,
      &PersistentConfig<16, 16, kMatchTable>::launch, nullptr},
     {"one tile per CTA, 8 warps x 16 items", PassConfig<uint32_t, 8, 16, 3, kMatchTable>::kTile,
      &PassConfig<uint32_t, 8, 16, 3, kMatchTable>::launch, &FreePassConfig<uint32_t, 8, 16, 4>::launch},
 };
-static_assert(FreePassConfig<uint32_t, 16, 16, 3>::kTile == PassConfig<uint32_t, 16, 16, 2, kMatchTable>::kTile &&
+static_assert(FreePassConfig<uint32_t, 16, 16, 3>::kTile == Variant0::kTile &&
                   FreePassConfig<uint32_t, 8, 16, 4>::kTile == PassConfig<uint32_t, 8, 16, 3, kMatchTable>::kTile,
               "an order-free first pass keeps its variant's tile");
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);

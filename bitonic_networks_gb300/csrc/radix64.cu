@@ -8,14 +8,16 @@
 namespace gsort {
 
 namespace {
-using Config64 = PassConfig<uint64_t, 16, 8, 2, kMatchTable>;
-using FreeConfig64 = FreePassConfig<uint64_t, 16, 8, 3>;   // the order-free first pass
-static_assert(FreeConfig64::kTile == Config64::kTile, "one tile size for every pass");
+using Keys64 = PassConfig<uint64_t, 16, 8, 3, kMatchTable>;    // keys only: three CTAs per SM
+using Config64 = PassConfig<uint64_t, 16, 8, 2, kMatchTable>;  // pairs: two
+using FreeConfig64 = FreePassConfig<uint64_t, 16, 8, 3>;       // the order-free first pass
+static_assert(FreeConfig64::kTile == Config64::kTile && Keys64::kTile == Config64::kTile,
+              "one tile size for every pass");
 }
 
 cudaError_t launch_pass_u64(const PassArgs &a, bool pairs, bool xin, bool xout, uint32_t tiles,
                             cudaStream_t s) {
-    return Config64::launch(a, pairs, xin, xout, tiles, s);
+    return pairs ? Config64::launch(a, pairs, xin, xout, tiles, s) : Keys64::launch_keys(a, pairs, xin, xout, tiles, s);
 }
 
 cudaError_t launch_pass_u64_free(const PassArgs &a, bool pairs, bool xin, bool xout, uint32_t tiles,

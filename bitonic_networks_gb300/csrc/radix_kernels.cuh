@@ -697,6 +697,20 @@ struct PassConfig {
         return byte ? launch_b<true>(a, pairs, xin, xout, tiles, s)
                     : launch_b<false>(a, pairs, xin, xout, tiles, s);
     }
+
+    // Keys only (instantiates no pairs kernel).
+    template <bool B>
+    static cudaError_t launch_kb(const PassArgs &a, bool xin, bool xout, uint32_t tiles, cudaStream_t s) {
+        if (xin) return xout ? launch_one<B, false, true, true>(a, tiles, s) : launch_one<B, false, true, false>(a, tiles, s);
+        return xout ? launch_one<B, false, false, true>(a, tiles, s) : launch_one<B, false, false, false>(a, tiles, s);
+    }
+
+    static cudaError_t launch_keys(const PassArgs &a, bool pairs, bool xin, bool xout, uint32_t tiles,
+                                   cudaStream_t s) {
+        if (pairs) return cudaErrorInvalidValue;
+        const bool byte = (a.shift % 8) == 0 && a.mask == 0xFFu;
+        return byte ? launch_kb<true>(a, xin, xout, tiles, s) : launch_kb<false>(a, xin, xout, tiles, s);
+    }
 };
 
 // ------------------------------------------- order-free first digit pass
