@@ -193,7 +193,7 @@ k_seg_hist(const uint32_t *__restrict__ keys, const SegTile *tiles, const uint32
 // before it claims the next), so the smallest unfinished tile can always
 // complete its look-back, whose chain ends at its segment's first tile.
 template <bool BYTE, bool PAIRS, bool XIN, bool XOUT>
-__global__ void __launch_bounds__(kSegPassWarps * 32, 2)
+__global__ void __launch_bounds__(kSegPassWarps * 32, PAIRS ? 2 : 3)
 k_seg_pass(const PassArgs a, const SegTile *tiles, const uint32_t *counts, const uint32_t *hist) {
     constexpr int T = kSegPassWarps * 32;
     constexpr int TILE = kSegTile;
@@ -491,7 +491,8 @@ int launch_segmented_sort(const SegLaunch &L) {
 
     // in -> tmp -> out -> tmp -> out (also when in == out: each pass reads
     // what the previous one wrote)
-    const uint32_t pgrid = std::max(1u, std::min(lay.tiles_max, sms * 2));
+    // keys-only passes fit three CTAs per SM (40 registers), pairs two
+    const uint32_t pgrid = std::max(1u, std::min(lay.tiles_max, sms * (pairs ? 2u : 3u)));
     const uint32_t *src_k = L.keys_in;
     const uint32_t *src_v = L.vals_in;
     for (int p = 0; p < 4; ++p) {
