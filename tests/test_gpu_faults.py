@@ -31,6 +31,20 @@ def test_radix_wait_gives_up_and_reports(stall, n):
     assert_bits_equal(host_u32(got), oracle.radix_sort_keys(k), "after timeout")
 
 
+# keys only, every bit: the first pass reserves bin places with atomic cursors
+# and waits for nothing; the stalled tile then never publishes in the second
+# pass, whose look-backs give up
+@pytest.mark.parametrize("stall", [0, 3])
+def test_keys_only_wait_gives_up_and_reports(stall):
+    n = 64 * 8192
+    k = synth.uniform_keys(n, 4)
+    with pytest.raises(gsort.GsortError) as e:
+        gsort.sort_pairs(dev(k), None, spin_limit=2000, stall_tile=stall)
+    assert e.value.code == ETIMEOUT
+    got = gsort.sort_keys(dev(k))
+    assert_bits_equal(host_u32(got), oracle.radix_sort_keys(k), "after timeout")
+
+
 @pytest.mark.parametrize("stall", [0, 2])
 def test_compaction_wait_gives_up_and_reports(stall):
     n = 8 * 8192

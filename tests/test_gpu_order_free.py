@@ -108,3 +108,13 @@ def test_segmented_keys_long_segments(shape):
     got, _ = gsort.segmented_sort(to_dev(k), to_dev(off), kind=0)
     exp, _ = oracle.default().segmented_sort_general(k, off, None, 0, False)
     assert np.array_equal(host_bytes(got), np.ascontiguousarray(exp).view(np.uint8))
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2])
+@pytest.mark.parametrize("shape", ["uniform", "low3", "distinct16"])
+def test_u32_keys_in_place(shape, variant):
+    k = keys32(shape, N, 7900 + SHAPES.index(shape))
+    t = to_dev(k)
+    got, _ = gsort.sort_pairs(t, None, 0, 32, keys_out=t, variant=variant)
+    assert got.data_ptr() == t.data_ptr()
+    assert np.array_equal(host_bytes(t), oracle.radix_sort_keys(k).view(np.uint8)), f"{shape} in place"
