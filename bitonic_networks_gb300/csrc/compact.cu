@@ -6,9 +6,12 @@
 // One kernel reads every tile once: predicate, block scan of the per-thread
 // counts, publish the tile count, look back (warp 0 inspects 32 earlier tiles
 // per step, while the other warps stage the tile's kept values contiguously in
-// shared memory) and copy the kept values out as one run.  The last tile records the total m; a second
-// kernel writes +0.0 to out[m..n) (the pages' worked example shows a zero
-// tail; their kernels leave it unwritten).  Traffic: read 4n, write 4n.
+// shared memory) and copy the kept values out as one run.  The output ends in
+// +0.0 from m to n (the pages' worked example shows a zero tail; their kernels
+// leave it unwritten): a tile with K kept values before it and z dropped ones
+// of its own writes its z zeros just below the zeros of the tiles before it,
+// at [n - (base - K) - z, n - (base - K)), so the tail fills from the end
+// without waiting for m.  The last tile records m.  Traffic: read 4n, write 4n.
 #include <algorithm>
 #include <mutex>
 
@@ -31,6 +34,20 @@ __global__ void k_zero_words(uint32_t *p, uint32_t nwords) {
         p[i] = 0;
 }
 
+// +0.0 into out[a, a + count): a head up to a 16-byte boundary, 16-byte
+// streaming stores, a tail.  Called by every thread of a block of T.
+template <int T>
+__device__ __forceinline__ void zero_run(uint32_t *out, uint32_t a, uint32_t count, uint32_t tid) {
+    uint32_t head = static_cast<uint32_t>(((16 - (reinterpret_cast<uintptr_t>(out + a) & 15)) & 15) >> 2);
+    head = min(head, count);
+    const uint32_t nvec = (count - head) >> 2;
+    uint4 *vec = reinterpret_cast<uint4 *>(out + a + head);
+    for (uint32_t v = tid; v < nvec; v += T) __stcs(vec + v, make_uint4(0, 0, 0, 0));
+    if (tid < head) out[a + tid] = 0;
+    const uint32_t tail0 = head + nvec * 4;
+    if (tid < count - tail0) out[a + tail0 + tid] = 0;
+}
+
 // x > 0 under IEEE comparison, on the bit pattern: sign clear, not +0, not
 // NaN (0 < bits <= 0x7F800000).  Positive subnormals count as positive.
 __device__ __forceinline__ uint32_t is_positive(uint32_t bits) {
@@ -41,7 +58,7 @@ template <int T, int IPT>
 __global__ void __launch_bounds__(T)
 k_compact(const uint32_t *__restrict__ in, uint32_t *__restrict__ out, uint32_t n,
           uint32_t *states, uint32_t *tile_counter, uint32_t *status, uint32_t *abort_flag,
-          unsigned long long *kept, uint32_t num_tiles, uint32_t spin_limit,
+          unsigned long long *kept, int64_t *num_kept, uint32_t num_tiles, uint32_t spin_limit,
           uint32_t stall_tile, int vec_ok) {
     constexpr uint32_t TILE = T * IPT;
     constexpr int WARPS = T / 32;
@@ -121,29 +138,17 @@ k_compact(const uint32_t *__restrict__ in, uint32_t *__restrict__ out, uint32_t 
         const uint32_t g = prefix + i;
         if (g < n) out[g] = s_buf[i];
     }
-    if (tile == num_tiles - 1 && tid == 0) *kept = static_cast<unsigned long long>(prefix) + total;
-}
-
-// +0.0 into out[m..n), m read from the workspace; also reports m.
-__global__ void k_zero_tail(uint32_t *out, uint32_t n, const unsigned long long *kept,
-                            int64_t *num_kept) {
-    __shared__ uint32_t s_m;
-    if (threadIdx.x == 0) s_m = static_cast<uint32_t>(min(*kept, static_cast<unsigned long long>(n)));
-    __syncthreads();
-    const uint32_t m = s_m;
-    if (blockIdx.x == 0 && threadIdx.x == 0 && num_kept != nullptr)
-        *num_kept = static_cast<int64_t>(m);
-    const uint32_t gtid = blockIdx.x * blockDim.x + threadIdx.x;
-    const uint32_t gstride = gridDim.x * blockDim.x;
-    // head up to a 16-byte boundary, vector body, tail
-    uint32_t head = static_cast<uint32_t>(((16 - (reinterpret_cast<uintptr_t>(out + m) & 15)) & 15) >> 2);
-    head = min(head, n - m);
-    const uint32_t nvec = (n - m - head) >> 2;
-    uint4 *vec = reinterpret_cast<uint4 *>(out + m + head);
-    for (uint32_t v = gtid; v < nvec; v += gstride) __stcs(vec + v, make_uint4(0, 0, 0, 0));
-    if (gtid < head) out[m + gtid] = 0;
-    const uint32_t tail0 = m + head + nvec * 4;
-    if (gtid < n - tail0) out[tail0 + gtid] = 0;
+    // this tile's share of the zero tail, below the shares of the tiles before it
+    if (prefix <= base) {   // guards the writes should a count ever be corrupt
+        const uint32_t dropped_before = base - prefix, dropped = tile_n - total;
+        if (static_cast<uint64_t>(dropped_before) + dropped <= n)
+            zero_run<T>(out, n - dropped_before - dropped, dropped, tid);
+    }
+    if (tile == num_tiles - 1 && tid == 0) {
+        const unsigned long long m = static_cast<unsigned long long>(prefix) + total;
+        *kept = m;
+        if (num_kept != nullptr) *num_kept = static_cast<int64_t>(m);
+    }
 }
 
 void record(cudaEvent_t *ev, int num, int idx, cudaStream_t s) {
@@ -179,14 +184,10 @@ int launch_compact(const CompactLaunch &L) {
 
     const int vec_ok = (reinterpret_cast<uintptr_t>(L.in) & 15) == 0;
     k_compact<kCompactThreads, kCompactItems><<<lay.tiles, kCompactThreads, 0, s>>>(
-        L.in, L.out, L.n, states, counter, status, abort_flag, kept, lay.tiles, L.spin_limit,
-        L.stall_tile, vec_ok);
+        L.in, L.out, L.n, states, counter, status, abort_flag, kept, L.num_kept, lay.tiles,
+        L.spin_limit, L.stall_tile, vec_ok);
     if (cudaGetLastError() != cudaSuccess) return GSORT_ECUDA;
-    record(L.events, L.num_events, 2, s);
-
-    const uint32_t tail_grid = std::max(1u, std::min<uint32_t>((L.n / 4 + 255) / 256, 8u * L.sm_count));
-    k_zero_tail<<<tail_grid, 256, 0, s>>>(L.out, L.n, kept, L.num_kept);
-    if (cudaGetLastError() != cudaSuccess) return GSORT_ECUDA;
+    record(L.events, L.num_events, 2, s);   // the zero tail is written by the same kernel
     record(L.events, L.num_events, 3, s);
     return GSORT_OK;
 }

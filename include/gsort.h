@@ -326,7 +326,8 @@ typedef struct gsort_options {
     /* Optional array of cudaEvent_t handles recorded on `stream` around the
      * launches: radix: [0] start, [1] after init, [2] after histogram,
      * [3 + p] after digit pass p; compaction: [0] start, [1] after init,
-     * [2] after the scan/scatter kernel, [3] after the zero fill.  Extra
+     * [2] and [3] after the scan/scatter kernel (which also writes the
+     * zero tail).  Extra
      * entries are left alone; missing ones are skipped. */
     void **events;
     int num_events;
@@ -370,7 +371,7 @@ const char *gsort_radix_variant_name(int variant);
  * accounting): radix: 2 for 32-bit keys and n <= 2^18 (one cooperative
  * kernel runs every pass), else 2 + passes (+1 copy-back when sorting in
  * place with an odd pass count; +1 histogram clear for 64-bit keys, see
- * gsort_radix_sort_launch_count); compaction: 3; segmented: 1 (0 when
+ * gsort_radix_sort_launch_count); compaction: 2; segmented: 1 (0 when
  * there is nothing to do). */
 int gsort_radix_launch_count(int64_t n, int begin_bit, int end_bit, int in_place);
 int gsort_radix_sort_launch_count(int64_t n, int kind, int begin_bit, int end_bit, int in_place);
