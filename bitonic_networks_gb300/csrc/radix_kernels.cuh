@@ -35,6 +35,16 @@
 // other warps' ranking, and the per-warp counters then hand out tile slots
 // directly; look-back words are cleared one row per tile by the previous
 // kernel instead of a memset per pass; every wait is bounded.
+//
+// Keys-only sorts over every bit of the key need less than full stability:
+// equal keys are identical, so a pass must keep the input order only between
+// keys that differ in the bits below its digit (by which its input is already
+// sorted).  Hence (both give the same output as the stable sort):
+//   - the first pass (k_digit_pass_free) ranks by one shared atomic per key
+//     and reserves each tile's places in the bins with atomic bin cursors, no
+//     multisplit and no look-back;
+//   - in later passes a warp whose keys agree below the digit (or take two
+//     values there) ranks by shared atomics instead of the multisplit.
 #pragma once
 
 #include <algorithm>
