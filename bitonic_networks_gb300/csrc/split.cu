@@ -112,7 +112,7 @@ __global__ void k_bit_zeros(const uint32_t *hist, uint32_t *zeros) {
 
 // ----------------------------------------------------------------- split
 template <class Pred, bool PAIRS>
-__global__ void __launch_bounds__(kSplitThreads)
+__global__ void __launch_bounds__(kSplitThreads, PAIRS ? 2 : 3)
 k_split(const uint32_t *__restrict__ in, const uint32_t *__restrict__ vin, uint32_t *__restrict__ out,
         uint32_t *__restrict__ vout, uint32_t n, Pred pred, const uint32_t *num_true,
         uint32_t *states, uint32_t *states_clear, uint32_t *tile_counter, uint32_t *status,
