@@ -55,7 +55,7 @@ __device__ __forceinline__ uint32_t is_positive(uint32_t bits) {
 }
 
 template <int T, int IPT>
-__global__ void __launch_bounds__(T)
+__global__ void __launch_bounds__(T, 4)
 k_compact(const uint32_t *__restrict__ in, uint32_t *__restrict__ out, uint32_t n,
           uint32_t *states, uint32_t *tile_counter, uint32_t *status, uint32_t *abort_flag,
           unsigned long long *kept, int64_t *num_kept, uint32_t num_tiles, uint32_t spin_limit,
