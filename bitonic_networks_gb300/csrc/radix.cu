@@ -175,18 +175,27 @@ struct PersistentConfig {
 
 // Keys and pairs in one variant with different occupancy: keys-only passes
 // fit 40 registers without spilling, so three CTAs share an SM; pairs hold
-// twice the registers per item and keep two.
-template <class KeysCfg, class PairsCfg>
+// twice the registers per item and keep two.  Keys-only passes whose runs of
+// equal low bits are expected to be short (under 256 keys for uniform input,
+// so most warps take the stable path: the last pass of a large sort) build
+// their peer masks with shared reductions (ShortRunsCfg), which costs less
+// integer work than the ballots on spread digits; elsewhere the ballot
+// tables, which do not serialise on repeated digits.
+template <class KeysCfg, class ShortRunsCfg, class PairsCfg>
 struct KeysPairsConfig {
-    static_assert(KeysCfg::kTile == PairsCfg::kTile, "one tile size per variant");
+    static_assert(KeysCfg::kTile == PairsCfg::kTile && ShortRunsCfg::kTile == KeysCfg::kTile,
+                  "one tile size per variant");
     static constexpr uint32_t kTile = KeysCfg::kTile;
     static cudaError_t launch(const PassArgs &a, bool pairs, bool xin, bool xout, uint32_t tiles,
                               cudaStream_t s) {
-        return pairs ? PairsCfg::launch(a, pairs, xin, xout, tiles, s)
-                     : KeysCfg::launch_keys(a, pairs, xin, xout, tiles, s);
+        if (pairs) return PairsCfg::launch(a, pairs, xin, xout, tiles, s);
+        return a.two_runs_ok ? KeysCfg::launch_keys(a, pairs, xin, xout, tiles, s)
+                             : ShortRunsCfg::launch_keys(a, pairs, xin, xout, tiles, s);
     }
 };
-using Variant0 = KeysPairsConfig<PassConfig<uint32_t, 16, 16, 3, kMatchTable>, PassConfig<uint32_t, 16, 16, 2, kMatchTable>>;
+using Variant0 = KeysPairsConfig<PassConfig<uint32_t, 16, 16, 3, kMatchTable>,
+                                 PassConfig<uint32_t, 16, 16, 3, kMatchRedOr>,
+                                 PassConfig<uint32_t, 16, 16, 2, kMatchTable>>;
 
 // `free_launch`: the first pass of a keys-only sort over every bit, where
 // every warp is order-free (same tile; null: the variant's own kernel, in its

@@ -274,7 +274,21 @@ k_digit_hist(const K *__restrict__ keys, uint32_t n, uint32_t begin_bit, int pas
 //                entries with two shuffles and ANDs them.
 //   kMatchSelect each lane selects, per bit, the ballot or its complement.
 //   kMatchAny    the hardware match.any instruction.
-constexpr int kMatchTable = 0, kMatchSelect = 1, kMatchAny = 2;
+constexpr int kMatchTable = 0, kMatchSelect = 1, kMatchAny = 2, kMatchRedOr = 3;
+// kMatchRedOr: each lane ORs its lane bit into a per-warp shared table entry
+// of its digit (a reduction, no value returned), reads the entry back after a
+// warp barrier, and the group's leader clears it.
+
+// Shared words of the per-warp peer tables of kMatchRedOr (after the misc words).
+template <int WARPS, int MATCH>
+__host__ __device__ constexpr size_t peer_table_words() {
+    return MATCH == kMatchRedOr ? static_cast<size_t>(WARPS) * 256 : 0;
+}
+
+__device__ __forceinline__ void red_or_shared(uint32_t *p, uint32_t v) {
+    asm volatile("red.shared.or.b32 [%0], %1;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(v)
+                 : "memory");
+}
 
 struct LaneConsts {
     uint32_t inv[5];   // ~0 where bit b of the lane id is 0, else 0
@@ -588,13 +602,25 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, cons
         for (int k = 0; k < IPT; ++k) {
             const bool valid = FULL || item0 + k * 32 < tile_n;
             const uint32_t d = valid ? digit_at<BYTE>(key[k], a.shift, a.mask) : 0u;
-            uint32_t peers = digit_peers<MATCH>(d, c);
-            if (!FULL) peers &= __ballot_sync(kFullMask, valid);
+            uint32_t peers;
+            if constexpr (MATCH == kMatchRedOr) {
+                uint32_t *pt = s_misc + 32 + warp * 256;   // this warp's peer table (zero between items)
+                if (valid) red_or_shared(&pt[d], 1u << lane);
+                __syncwarp();
+                peers = valid ? pt[d] : 0u;
+                __syncwarp();   // every lane has read its entry before the leaders clear them
+            } else {
+                peers = digit_peers<MATCH>(d, c);
+                if (!FULL) peers &= __ballot_sync(kFullMask, valid);
+            }
             const uint32_t leader = highest_bit(peers);   // peers is empty only for padding lanes
             uint32_t base = 0;
-            if (valid && lane == leader)
+            if (valid && lane == leader) {
                 base = atomicAdd(&wc[d], static_cast<uint32_t>(__popc(peers)));
+                if constexpr (MATCH == kMatchRedOr) s_misc[32 + warp * 256 + d] = 0u;
+            }
             base = __shfl_sync(kFullMask, base, leader);
+            if constexpr (MATCH == kMatchRedOr) __syncwarp();   // cleared before the next item's reductions
             if (valid) {
                 const uint32_t slot = base + __popc(peers & ltm);
                 s_keys[slot] = key[k];
@@ -640,6 +666,8 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass(const PassArgs 
     constexpr size_t kKeyWords = sizeof(K) / 4;
     uint32_t *s_cnt = smem + TILE * (kKeyWords + (PAIRS ? 1 : 0));
     for (uint32_t i = tid; i < WARPS * kRow; i += WARPS * 32) s_cnt[i] = 0;
+    if constexpr (MATCH == kMatchRedOr)
+        for (uint32_t i = tid; i < peer_table_words<WARPS, MATCH>(); i += WARPS * 32) s_misc[32 + i] = 0;
     __syncthreads();
     const uint32_t tile = s_misc[0];
     if (s_misc[1]) return;   // an earlier wait gave up; the result is void anyway
@@ -678,7 +706,7 @@ struct PassConfig {
     template <bool B, bool P, bool XI, bool XO>
     static cudaError_t launch_one(const PassArgs &a, uint32_t tiles, cudaStream_t s) {
         auto k = k_digit_pass<K, WARPS, IPT, MINB, MATCH, LW, B, P, XI, XO>;
-        const size_t smem = pass_smem_words<K, WARPS, IPT, P>() * sizeof(uint32_t);
+        const size_t smem = (pass_smem_words<K, WARPS, IPT, P>() + peer_table_words<WARPS, MATCH>()) * sizeof(uint32_t);
         cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(k), smem);
         if (e != cudaSuccess) return e;
         k<<<tiles, WARPS * 32, smem, s>>>(a);
