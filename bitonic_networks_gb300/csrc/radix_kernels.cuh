@@ -44,7 +44,10 @@
 //     and reserves each tile's places in the bins with atomic bin cursors, no
 //     multisplit and no look-back;
 //   - in later passes a warp whose keys agree below the digit (or take two
-//     values there) ranks by shared atomics instead of the multisplit.
+//     values there) ranks by shared atomics instead of the multisplit;
+//   - where such runs are short (most warps stable), the multisplit's peer
+//     masks come from shared OR-reductions into per-warp tables (kMatchRedOr)
+//     instead of ballots: less integer work, more shared-memory traffic.
 #pragma once
 
 #include <algorithm>
