@@ -201,6 +201,7 @@ struct RadixLaunch {
 // Layout of the radix workspace after the header.
 struct RadixLayout {
     uint32_t tiles_max;   // tiles of the smallest tile size any variant uses
+    size_t starts;        // u32[8][256] bin starts of every pass (exclusive scans of the histograms)
     size_t hist;          // u32[passes][256] digit histograms
     size_t look_a, look_b;  // [tiles_max][256] look-back words, alternating between passes
     size_t tmp_keys, tmp_vals;

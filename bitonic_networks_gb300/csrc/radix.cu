@@ -249,6 +249,8 @@ RadixLayout radix_layout(uint32_t n, bool with_values, int key_bytes) {
     RadixLayout L{};
     L.tiles_max = (n + kMinRadixTile - 1) / kMinRadixTile;
     size_t off = kHdrBytes;
+    L.starts = off;   // bin starts of up to 8 passes
+    off += align_up(8 * 256 * sizeof(uint32_t), kWsAlign);
     // 32-bit keys keep their 4 x 256 histogram counts in the header; 64-bit
     // keys have 8 passes and take a region of their own
     L.hist = key_bytes == 8 ? off : kHdrHist;
@@ -306,6 +308,8 @@ int launch_radix(const RadixLaunch &L) {
     uint32_t *status = reinterpret_cast<uint32_t *>(L.ws + kHdrStatus);
     uint32_t *abort_flag = reinterpret_cast<uint32_t *>(L.ws + kHdrAbort);
     uint32_t *hist = reinterpret_cast<uint32_t *>(L.ws + lay.hist);
+    uint32_t *starts = reinterpret_cast<uint32_t *>(L.ws + lay.starts);
+    uint32_t *cursor = reinterpret_cast<uint32_t *>(L.ws + kHdrCursor);
     uint32_t *look[2] = {reinterpret_cast<uint32_t *>(L.ws + lay.look_a),
                          reinterpret_cast<uint32_t *>(L.ws + lay.look_b)};
     void *tmp_k = L.ws + lay.tmp_keys;
@@ -358,6 +362,11 @@ int launch_radix(const RadixLaunch &L) {
     if (launch_hist_any(L.keys_in, L.n, order, L.begin_bit, passes, last_mask, hist, look[0],
                         tiles * 256, s, L.sm_count) != cudaSuccess)
         return GSORT_ECUDA;
+    // keys only, every bit: equal keys are indistinguishable, so a warp needs
+    // stable ranks only where its keys differ below the current digit
+    const bool order_free = !pairs && L.begin_bit == 0 && L.end_bit == static_cast<int>(8 * kb);
+    k_bin_starts<<<1, 256, 0, s>>>(hist, passes, starts, order_free ? cursor : nullptr);
+    if (cudaGetLastError() != cudaSuccess) return GSORT_ECUDA;
     record(L.events, L.num_events, 2, s);
 
     // In place (either array): in -> tmp -> out -> tmp ...; an odd pass count
@@ -393,14 +402,13 @@ int launch_radix(const RadixLaunch &L) {
         const bool src16 = (reinterpret_cast<uintptr_t>(src_k) & 15) == 0 &&
                            (!pairs || (reinterpret_cast<uintptr_t>(src_v) & 15) == 0);
         a.prefetch_dist = src16 ? 2u * static_cast<uint32_t>(L.sm_count) : 0u;
-        // keys only, every bit: equal keys are indistinguishable, so a warp
-        // needs stable ranks only where its keys differ below this digit
-        a.order_free = (!pairs && L.begin_bit == 0 && L.end_bit == static_cast<int>(8 * kb)) ? 1u : 0u;
+        a.order_free = order_free ? 1u : 0u;
         a.free_low = a.shift >= 64 ? ~0ull : ((1ull << a.shift) - 1ull);
         // runs of equal low bits hold about n / 2^shift keys of uniform input;
         // below half a warp's keys (512), two-value warps are rare
         a.two_runs_ok = (a.shift < 32 && (static_cast<uint64_t>(L.n) >> a.shift) >= 256) ? 1u : 0u;
-        a.cursor = (a.order_free && p == 0) ? reinterpret_cast<uint32_t *>(L.ws + kHdrCursor) : nullptr;
+        a.cursor = (a.order_free && p == 0) ? cursor : nullptr;
+        a.start = starts + p * 256;
         const bool xin = mapped && p == 0;
         const bool xout = mapped && p == passes - 1;
         const PassLauncher use = a.cursor != nullptr && free_launch != nullptr ? free_launch : launch;

@@ -90,8 +90,12 @@ struct PassArgs {
     // Non-null (first pass of such a sort, where every warp is order-free):
     // any tile may take any place inside a digit's bin, so a tile reserves
     // its places with one atomic add per digit on these 256 bin cursors
-    // (zeroed) instead of looking back, and takes its tile by block index.
+    // (each set to its bin's start) instead of looking back, and takes its
+    // tile by block index.
     uint32_t *cursor = nullptr;
+    // Non-null: the bin starts of this pass (the exclusive scan of `hist`,
+    // written by k_bin_starts), so that no tile scans the 256 counts again.
+    const uint32_t *start = nullptr;
 };
 
 // Launch of one digit pass over `tiles` tiles (one configuration of the kernel).
@@ -507,15 +511,17 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, cons
         }
         if (tile != a.stall_tile && a.cursor == nullptr)
             st_relaxed(a.look + tile * 256 + tid, (tile == td.first ? kFlagPrefix : kFlagAgg) | cnt);
-        const uint32_t bin = td.hist[tid];
         const uint32_t ic = warp_inclusive_scan(cnt, lane);
-        const uint32_t ib = warp_inclusive_scan(bin, lane);
-        if (lane == 31) {
-            s_misc[4 + warp] = ic;
-            s_misc[12 + warp] = ib;
-        }
+        if (lane == 31) s_misc[4 + warp] = ic;
         tile_excl = ic - cnt;
-        bin_excl = ib - bin;
+        if (a.start != nullptr) {
+            bin_excl = a.start[tid];
+        } else {   // per-segment counts: scan them here
+            const uint32_t bin = td.hist[tid];
+            const uint32_t ib = warp_inclusive_scan(bin, lane);
+            if (lane == 31) s_misc[12 + warp] = ib;
+            bin_excl = ib - bin;
+        }
     }
     if (a.look_clear != nullptr)
         for (uint32_t i = tid; i < 256; i += T) a.look_clear[tile * 256 + i] = 0;
@@ -523,7 +529,7 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, cons
     if (tid < 256) {
         for (uint32_t w = 0; w < warp; ++w) {
             tile_excl += s_misc[4 + w];
-            bin_excl += s_misc[12 + w];
+            if (a.start == nullptr) bin_excl += s_misc[12 + w];
         }
         // s_cnt[w][d]: tile slot where warp w's first key of digit d goes
 #pragma unroll
@@ -546,8 +552,9 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, cons
             s_misc[2] = 1;
             record_error(a.status, a.abort_flag, GSORT_ETIMEOUT);
         }
-        // global index of tile slot i holding digit d: s_goff[d] + i
-        s_goff[tid] = td.out_base + bin_excl + excl - tile_excl;
+        // global index of tile slot i holding digit d: s_goff[d] + i (a bin
+        // cursor already holds its bin's start)
+        s_goff[tid] = td.out_base + (a.cursor != nullptr ? 0u : bin_excl) + excl - tile_excl;
     }
 
     // ---- order-free warps: the warp's keys are sorted by the bits below this
@@ -652,6 +659,27 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, cons
     return true;
 }
 
+// The CTA that takes tile + prefetch_dist (about one CTA lifetime later)
+// then finds its keys in L2 instead of waiting for HBM: one bulk L2 prefetch
+// of that tile's keys (and values), issued by one thread.  Sources must be
+// 16-byte aligned (prefetch_dist is 0 otherwise).
+template <class K, int TILE, bool PAIRS>
+__device__ __forceinline__ void prefetch_tile_l2(const PassArgs &a, uint32_t tile) {
+    if (a.prefetch_dist == 0) return;
+    const uint32_t pt = tile + a.prefetch_dist;
+    if (pt >= (a.n + TILE - 1) / TILE) return;
+    const uint32_t cnt = min(static_cast<uint32_t>(TILE), a.n - pt * TILE);
+    const uint32_t kbytes = (cnt * static_cast<uint32_t>(sizeof(K))) & ~15u;
+    if (kbytes)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                     ::"l"(static_cast<const K *>(a.src_k) + static_cast<size_t>(pt) * TILE), "r"(kbytes)
+                     : "memory");
+    const uint32_t vbytes = (cnt * 4u) & ~15u;
+    if (PAIRS && vbytes)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                     ::"l"(a.src_v + static_cast<size_t>(pt) * TILE), "r"(vbytes) : "memory");
+}
+
 template <class K, int WARPS, int IPT, int MINB, int MATCH, int LW, bool BYTE, bool PAIRS, bool XIN,
           bool XOUT>
 __global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass(const PassArgs a) {
@@ -674,22 +702,7 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass(const PassArgs 
     __syncthreads();
     const uint32_t tile = s_misc[0];
     if (s_misc[1]) return;   // an earlier wait gave up; the result is void anyway
-    if (tid == 0 && a.prefetch_dist != 0) {
-        // The CTA that claims tile + prefetch_dist (about one CTA lifetime
-        // later) then finds its keys in L2 instead of waiting for HBM.
-        const uint32_t pt = tile + a.prefetch_dist;
-        if (pt < (a.n + TILE - 1) / TILE) {
-            const uint32_t cnt = min(static_cast<uint32_t>(TILE), a.n - pt * TILE);
-            const uint32_t kbytes = (cnt * static_cast<uint32_t>(sizeof(K))) & ~15u;
-            if (kbytes)
-                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
-                             ::"l"(static_cast<const K *>(a.src_k) + pt * TILE), "r"(kbytes) : "memory");
-            const uint32_t vbytes = (cnt * 4u) & ~15u;
-            if (PAIRS && vbytes)
-                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
-                             ::"l"(a.src_v + pt * TILE), "r"(vbytes) : "memory");
-        }
-    }
+    if (tid == 0) prefetch_tile_l2<K, TILE, PAIRS>(a, tile);
     K *s_keys = reinterpret_cast<K *>(smem);
     uint32_t *s_vals = smem + TILE * kKeyWords;
     const K *kin = static_cast<const K *>(a.src_k) + tile * TILE;
@@ -765,7 +778,10 @@ struct PassConfig {
 //     add per digit on 256 bin cursors (no look-back, no wait on any other
 //     tile), and takes its tile by block index;
 //   - the tile is reordered in shared memory and written as per-digit runs,
-//     as in the stable pass.
+//     as in the stable pass;
+//   - since the order inside the tile does not matter, a full, 16-byte
+//     aligned tile comes in 16-byte loads ([CUDA3] vector access), and each
+//     CTA asks L2 for the keys of the tile one CTA lifetime ahead.
 // Shared memory: keys of the tile, 256 counts/tile offsets, 256 global
 // offsets, 32 misc words.
 template <class K, int WARPS, int IPT>
@@ -773,7 +789,7 @@ __host__ __device__ constexpr size_t free_pass_smem_words() {
     return static_cast<size_t>(WARPS * 32 * IPT) * (sizeof(K) / 4) + 256 + 256 + 32;
 }
 
-template <class K, int WARPS, int IPT, int MINB, bool BYTE, bool XIN, bool XOUT>
+template <class K, int WARPS, int IPT, int MINB, bool BYTE, bool XIN, bool XOUT, bool VEC = true>
 __global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass_free(const PassArgs a) {
     static_assert(WARPS * 32 >= 256, "one thread per digit");
     static_assert(IPT % 2 == 0, "ranks are packed two per register");
@@ -789,16 +805,42 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass_free(const Pass
     const uint32_t tile_n = min(static_cast<uint32_t>(TILE), a.n - tile * TILE);
     const K *kin = static_cast<const K *>(a.src_k) + static_cast<size_t>(tile) * TILE;
 
-    // keys first (their latency overlaps the table set-up)
+    // keys first (their latency overlaps the table set-up); the order of the
+    // keys inside the tile does not matter here, so a full tile of 16-byte
+    // aligned keys comes in 16-byte loads
     K key[IPT];
+    constexpr int kPerVec = 16 / sizeof(K);
+    if (VEC && tile_n == static_cast<uint32_t>(TILE) && (reinterpret_cast<uintptr_t>(kin) & 15) == 0) {
+        const uint4 *kv = reinterpret_cast<const uint4 *>(kin);
 #pragma unroll
-    for (int k = 0; k < IPT; ++k) {
-        const uint32_t i = k * T + tid;
-        key[k] = i < tile_n ? kin[i] : K(0);
-        if (XIN) key[k] = order_in<K>(key[k], static_cast<K>(a.fmask), static_cast<K>(a.flip));
+        for (int j = 0; j < IPT / kPerVec; ++j) {
+            const uint4 q = __ldcs(kv + j * T + tid);
+            if constexpr (sizeof(K) == 4) {
+                key[4 * j] = q.x;
+                key[4 * j + 1] = q.y;
+                key[4 * j + 2] = q.z;
+                key[4 * j + 3] = q.w;
+            } else {
+                key[2 * j] = (static_cast<uint64_t>(q.y) << 32) | q.x;
+                key[2 * j + 1] = (static_cast<uint64_t>(q.w) << 32) | q.z;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < IPT; ++k) {
+            const uint32_t i = k * T + tid;
+            key[k] = i < tile_n ? kin[i] : K(0);
+        }
+    }
+    if (XIN) {
+#pragma unroll
+        for (int k = 0; k < IPT; ++k) key[k] = order_in<K>(key[k], static_cast<K>(a.fmask), static_cast<K>(a.flip));
     }
     if (tid < 256) s_cnt[tid] = 0;
-    if (tid == 0) s_misc[0] = ld_relaxed(a.abort_flag);
+    if (tid == 0) {
+        s_misc[0] = ld_relaxed(a.abort_flag);
+        prefetch_tile_l2<K, TILE, false>(a, tile);
+    }
     __syncthreads();
     if (s_misc[0]) return;   // an earlier wait gave up; the result is void anyway
 
@@ -828,26 +870,17 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass_free(const Pass
     }
     __syncthreads();
 
-    // scans over the 256 digits: tile offsets and bin starts
-    uint32_t cnt = 0, tile_excl = 0, bin_excl = 0;
+    // scan over the 256 digits: tile offsets (the bin starts are in the cursors)
+    uint32_t cnt = 0, tile_excl = 0;
     if (tid < 256) {
         cnt = s_cnt[tid];
-        const uint32_t bin = a.hist[tid];
         const uint32_t ic = warp_inclusive_scan(cnt, lane);
-        const uint32_t ib = warp_inclusive_scan(bin, lane);
-        if (lane == 31) {
-            s_misc[4 + warp] = ic;
-            s_misc[12 + warp] = ib;
-        }
+        if (lane == 31) s_misc[4 + warp] = ic;
         tile_excl = ic - cnt;
-        bin_excl = ib - bin;
     }
     __syncthreads();
     if (tid < 256) {
-        for (uint32_t w = 0; w < warp; ++w) {
-            tile_excl += s_misc[4 + w];
-            bin_excl += s_misc[12 + w];
-        }
+        for (uint32_t w = 0; w < warp; ++w) tile_excl += s_misc[4 + w];
         s_cnt[tid] = tile_excl;
     }
     __syncthreads();
@@ -864,7 +897,7 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass_free(const Pass
             s_keys[s_cnt[digit_at<BYTE>(key[k], a.shift, a.mask)] + r] = key[k];
         }
     }
-    if (tid < 256) s_goff[tid] = bin_excl + excl - tile_excl;
+    if (tid < 256) s_goff[tid] = excl - tile_excl;   // the cursor started at the bin's start
     __syncthreads();
     if (tile == a.stall_tile) return;
 
@@ -912,6 +945,30 @@ struct FreePassConfig {
         return byte ? launch_b<true>(a, xin, xout, tiles, s) : launch_b<false>(a, xin, xout, tiles, s);
     }
 };
+
+// ------------------------------------------------------ bin starts
+// After the histogram ([CUDA3] kernel 2; [PMPP10] 10.3): the exclusive scan of
+// every pass's 256 counts, so that no tile scans them again, and (keys-only
+// sorts over every bit) the first pass's bin cursors set to its bin starts.
+// One CTA of 256 threads, one digit each.
+__global__ void __launch_bounds__(256) k_bin_starts(const uint32_t *__restrict__ hist, int passes,
+                                                    uint32_t *__restrict__ start,
+                                                    uint32_t *__restrict__ cursor) {
+    __shared__ uint32_t s_sum[8];
+    const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int p = 0; p < passes; ++p) {
+        const uint32_t h = hist[p * 256 + tid];
+        const uint32_t inc = warp_inclusive_scan(h, lane);
+        if (lane == 31) s_sum[warp] = inc;
+        __syncthreads();
+        uint32_t base = 0;
+        for (uint32_t w = 0; w < warp; ++w) base += s_sum[w];
+        const uint32_t st = base + inc - h;
+        start[p * 256 + tid] = st;
+        if (p == 0 && cursor != nullptr) cursor[tid] = st;
+        __syncthreads();
+    }
+}
 
 // Histogram launch: one CTA per SM (fewer for small inputs: about 16 keys per
 // thread at least).

@@ -1,6 +1,6 @@
 """Runs one library call on a seeded input, for profilers (ncu).
 
-    python -m bitonic_networks_gb300.profile_cases OP [--n-log2 K] [--warmup W]
+    python profile_cases.py OP [--n-log2 K] [--warmup W]
            [--reps R] [--variant V]
 
 OP: keys (uint32 keys, 32 bits), pairs (uint32 key/index pairs), fpairs
@@ -17,12 +17,15 @@ any error, so a profiler only ever runs a command that finished cleanly.
 from __future__ import annotations
 
 import argparse
+import os
 import sys
 
 import numpy as np
 import torch
 
-from . import _lib, gsort, synth
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+
+from bitonic_networks_gb300 import _lib, gsort, synth
 
 
 def main(argv=None) -> int:

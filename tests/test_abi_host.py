@@ -63,8 +63,9 @@ def test_workspace_sizes(lib):
         keys = up(n * 4)
         # up to 2^18 keys: three count buffers of the one-launch sort, a row per 2048 keys
         small = up(3 * ((n + 2047) // 2048) * 1024) if n <= 1 << 18 else 0
-        assert lib.gsort_radix_workspace_bytes(n, 0) == HDR + state + keys + small
-        assert lib.gsort_radix_workspace_bytes(n, 1) == HDR + state + 2 * keys + small
+        starts = 8 * 1024   # bin starts of up to 8 passes
+        assert lib.gsort_radix_workspace_bytes(n, 0) == HDR + starts + state + keys + small
+        assert lib.gsort_radix_workspace_bytes(n, 1) == HDR + starts + state + 2 * keys + small
         ctiles = (n + 8191) // 8192
         assert lib.gsort_compact_workspace_bytes(n) == HDR + up(ctiles * 128)   # a line per tile
     assert lib.gsort_radix_workspace_bytes(-1, 0) == 0
@@ -84,10 +85,10 @@ def test_general_workspace_sizes(lib):
             for wv in (0, 1):
                 assert lib.gsort_radix_sort_workspace_bytes(n, kind, wv) == \
                     lib.gsort_radix_workspace_bytes(n, wv)
-        for kind in (3, 4, 5):     # 64-bit kinds: 8 KiB of histograms, 8-byte keys
-            assert lib.gsort_radix_sort_workspace_bytes(n, kind, 0) == HDR + 8192 + state + up(8 * n)
+        for kind in (3, 4, 5):     # 64-bit kinds: 8 KiB of bin starts and 8 KiB of histograms, 8-byte keys
+            assert lib.gsort_radix_sort_workspace_bytes(n, kind, 0) == HDR + 2 * 8192 + state + up(8 * n)
             assert lib.gsort_radix_sort_workspace_bytes(n, kind, 1) == \
-                HDR + 8192 + state + up(8 * n) + up(4 * n)
+                HDR + 2 * 8192 + state + up(8 * n) + up(4 * n)
     assert lib.gsort_radix_sort_workspace_bytes(10, 6, 0) == 0
     assert lib.gsort_radix_sort_workspace_bytes(10, -1, 0) == 0
     assert lib.gsort_radix_sort_workspace_bytes(1 << 30, 3, 0) == 0
@@ -173,14 +174,15 @@ def test_partition_and_split_sort_argument_errors(lib):
 def test_launch_count(lib):
     assert lib.gsort_radix_launch_count(100, 0, 32, 0) == 2          # small input: one cooperative kernel
     assert lib.gsort_radix_launch_count(1 << 18, 0, 32, 1) == 2
-    assert lib.gsort_radix_launch_count((1 << 18) + 1, 0, 32, 0) == 6
-    assert lib.gsort_radix_launch_count(1 << 20, 0, 8, 0) == 3
-    assert lib.gsort_radix_launch_count(1 << 20, 0, 24, 1) == 6
+    # header clear, histogram, bin starts, the passes
+    assert lib.gsort_radix_launch_count((1 << 18) + 1, 0, 32, 0) == 7
+    assert lib.gsort_radix_launch_count(1 << 20, 0, 8, 0) == 4
+    assert lib.gsort_radix_launch_count(1 << 20, 0, 24, 1) == 7
     assert lib.gsort_radix_launch_count(0, 0, 32, 0) == 0
     assert lib.gsort_radix_launch_count(100, 5, 5, 0) == 0
-    assert lib.gsort_radix_sort_launch_count(100, 3, 0, 64, 0) == 11      # 2 + 8 passes + hist clear
-    assert lib.gsort_radix_sort_launch_count(100, 5, 0, 56, 1) == 11      # 7 passes, in place: + copy
-    assert lib.gsort_radix_sort_launch_count(1 << 20, 2, 0, 32, 0) == 6
+    assert lib.gsort_radix_sort_launch_count(100, 3, 0, 64, 0) == 12      # 3 + 8 passes + hist clear
+    assert lib.gsort_radix_sort_launch_count(100, 5, 0, 56, 1) == 12      # 7 passes, in place: + copy
+    assert lib.gsort_radix_sort_launch_count(1 << 20, 2, 0, 32, 0) == 7
     assert lib.gsort_radix_sort_launch_count(100, 2, 0, 32, 0) == 2
 
 
