@@ -20,6 +20,7 @@ constexpr int kNumCounters = 8;
 constexpr size_t kHdrKept = kHdrCounters + 128 * kNumCounters;  // u64 kept count (compaction)
 constexpr size_t kHdrHist = 2048;     // u32[4][256] digit histograms (radix, 32-bit keys)
 constexpr size_t kHdrCursor = kHdrHist + 4096;   // u32[256] bin cursors of an order-free first pass (radix)
+constexpr size_t kHdrHot = kHdrCursor + 1024;    // u32[8] most frequent digit of each pass (radix)
 constexpr size_t kHdrBytes = 8192;    // header size, keeps what follows 256-byte aligned
 constexpr size_t kWsAlign = 256;
 

@@ -82,7 +82,10 @@ __global__ void __launch_bounds__(WARPS * 32, 2) k_digit_pass_persistent(const P
     uint32_t b = 0;
     uint32_t phase[2] = {0u, 0u};
     while (tile < tiles) {
-        if (tid == 0) s_misc[2] = 0;
+        if (tid == 0) {
+            s_misc[2] = 0;
+            s_misc[3] = a.hot != nullptr ? *a.hot : 256u;
+        }
         for (uint32_t i = tid; i < WARPS * kRow; i += T) tab[i] = 0;
         const bool arrived = mbar_wait_bounded(&bar[b], phase[b], kBulkWaitLimit);
         const uint32_t tile_n = min(static_cast<uint32_t>(TILE), a.n - tile * TILE);
@@ -365,7 +368,8 @@ int launch_radix(const RadixLaunch &L) {
     // keys only, every bit: equal keys are indistinguishable, so a warp needs
     // stable ranks only where its keys differ below the current digit
     const bool order_free = !pairs && L.begin_bit == 0 && L.end_bit == static_cast<int>(8 * kb);
-    k_bin_starts<<<1, 256, 0, s>>>(hist, passes, starts, order_free ? cursor : nullptr);
+    uint32_t *hot = reinterpret_cast<uint32_t *>(L.ws + kHdrHot);
+    k_bin_starts<<<1, 256, 0, s>>>(hist, passes, L.n, starts, order_free ? cursor : nullptr, hot);
     if (cudaGetLastError() != cudaSuccess) return GSORT_ECUDA;
     record(L.events, L.num_events, 2, s);
 
@@ -409,6 +413,7 @@ int launch_radix(const RadixLaunch &L) {
         a.two_runs_ok = (a.shift < 32 && (static_cast<uint64_t>(L.n) >> a.shift) >= 256) ? 1u : 0u;
         a.cursor = (a.order_free && p == 0) ? cursor : nullptr;
         a.start = starts + p * 256;
+        a.hot = hot + p;
         const bool xin = mapped && p == 0;
         const bool xout = mapped && p == passes - 1;
         const PassLauncher use = a.cursor != nullptr && free_launch != nullptr ? free_launch : launch;

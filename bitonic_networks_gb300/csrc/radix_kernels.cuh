@@ -96,6 +96,9 @@ struct PassArgs {
     // Non-null: the bin starts of this pass (the exclusive scan of `hist`,
     // written by k_bin_starts), so that no tile scans the 256 counts again.
     const uint32_t *start = nullptr;
+    // Non-null: the pass's most frequent digit if it holds more than 1/8 of
+    // the keys, else 256 (written by k_bin_starts).
+    const uint32_t *hot = nullptr;
 };
 
 // Launch of one digit pass over `tiles` tiles (one configuration of the kernel).
@@ -373,6 +376,27 @@ __device__ __forceinline__ uint32_t take_slot(uint32_t *tab, uint32_t d, uint32_
     return atomicAdd(&tab[d], 1u);
 }
 
+// Next free slot of digit d for this lane's key (order free), where `hot` is
+// the pass's most frequent digit: the lanes holding it take their slots with
+// one atomic of the lowest such lane, since same-address atomics that return
+// a value serialise across the lanes and skewed inputs can put a third of a
+// warp's keys on one digit.  Lanes with valid == false take nothing (every
+// lane of the warp must call this).
+__device__ __forceinline__ uint32_t take_slot_hot(uint32_t *tab, uint32_t d, uint32_t hot, uint32_t lane,
+                                                  bool valid) {
+    const bool h = valid && d == hot;
+    const uint32_t hm = __ballot_sync(kFullMask, h);
+    uint32_t r = 0;
+    if (hm != 0) {   // the same in every lane
+        const uint32_t leader = __ffs(hm) - 1;
+        uint32_t base = 0;
+        if (lane == leader) base = atomicAdd(&tab[hot], static_cast<uint32_t>(__popc(hm)));
+        r = __shfl_sync(kFullMask, base, leader) + __popc(hm & lanemask_lt());
+    }
+    if (valid && !h) r = atomicAdd(&tab[d], 1u);
+    return r;
+}
+
 constexpr int kRow = 256;   // per-warp digit counters
 
 template <class K, int WARPS, int IPT, bool PAIRS>
@@ -439,7 +463,8 @@ __device__ __forceinline__ bool look_back(const PassArgs &a, const TileDesc &td,
 // global memory, or in a shared staging buffer); the tile-sorted keys/values
 // go to s_keys/s_vals (which may be the staging buffers: every key is in
 // registers before the first write).  tab = the shared tables: per-warp digit
-// counters, digit offsets, misc words.  before_output() runs in every thread
+// counters, digit offsets, misc words; the kernel sets misc word 2 to 0 and
+// misc word 3 to the pass's skewed digit (256: none) before the call.  before_output() runs in every thread
 // after the last block barrier, before the output phase.  Returns false when
 // the tile stops (device error or the test stall), after that barrier.
 struct NoHook {
@@ -586,7 +611,12 @@ __device__ __forceinline__ bool pass_tile(const PassArgs &a, uint32_t *tab, cons
     }
     if (order_free) {
         uint32_t *wc = s_cnt + warp * kRow;
-        if (!two_runs) {
+        const uint32_t hot = s_misc[3];   // the pass's skewed digit (256: none), set by the kernel
+        if (hot < 256u && !one_digit && !two_runs) {   // skewed digits (the same in every thread of the grid)
+#pragma unroll
+            for (int k = 0; k < IPT; ++k)
+                s_keys[take_slot_hot(wc, digit_at<BYTE>(key[k], a.shift, a.mask), hot, lane, true)] = key[k];
+        } else if (!two_runs) {
 #pragma unroll
             for (int k = 0; k < IPT; ++k)   // order-free warps come from full tiles only
                 s_keys[take_slot(wc, digit_at<BYTE>(key[k], a.shift, a.mask), lane, one_digit)] = key[k];
@@ -693,6 +723,7 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass(const PassArgs 
         s_misc[0] = a.cursor != nullptr ? blockIdx.x : atomicAdd(a.tile_counter, 1u);
         s_misc[1] = ld_relaxed(a.abort_flag);
         s_misc[2] = 0;
+        s_misc[3] = a.hot != nullptr ? *a.hot : 256u;
     }
     constexpr size_t kKeyWords = sizeof(K) / 4;
     uint32_t *s_cnt = smem + TILE * (kKeyWords + (PAIRS ? 1 : 0));
@@ -805,6 +836,7 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass_free(const Pass
     const uint32_t tile_n = min(static_cast<uint32_t>(TILE), a.n - tile * TILE);
     const K *kin = static_cast<const K *>(a.src_k) + static_cast<size_t>(tile) * TILE;
 
+    const uint32_t hot = a.hot != nullptr ? *a.hot : 256u;   // the pass's skewed digit; 256: none
     // keys first (their latency overlaps the table set-up); the order of the
     // keys inside the tile does not matter here, so a full tile of 16-byte
     // aligned keys comes in 16-byte loads
@@ -855,18 +887,29 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass_free(const Pass
         one_digit = __all_sync(kFullMask, same);
     }
     uint32_t rk[IPT / 2];
+    if (hot < 256u && !one_digit) {   // the same in every thread of the grid
 #pragma unroll
-    for (int k = 0; k < IPT; k += 2) {
-        uint32_t r0 = 0, r1 = 0;
-        if (one_digit) {
-            r0 = take_slot(s_cnt, digit_at<BYTE>(key[k], a.shift, a.mask), lane, true);
-            r1 = take_slot(s_cnt, digit_at<BYTE>(key[k + 1], a.shift, a.mask), lane, true);
-        } else {
-            if (k * T + tid < tile_n) r0 = atomicAdd(&s_cnt[digit_at<BYTE>(key[k], a.shift, a.mask)], 1u);
-            if ((k + 1) * T + tid < tile_n)
-                r1 = atomicAdd(&s_cnt[digit_at<BYTE>(key[k + 1], a.shift, a.mask)], 1u);
+        for (int k = 0; k < IPT; k += 2) {
+            const uint32_t r0 = take_slot_hot(s_cnt, digit_at<BYTE>(key[k], a.shift, a.mask), hot, lane,
+                                              k * T + tid < tile_n);
+            const uint32_t r1 = take_slot_hot(s_cnt, digit_at<BYTE>(key[k + 1], a.shift, a.mask), hot, lane,
+                                              (k + 1) * T + tid < tile_n);
+            rk[k / 2] = r0 | (r1 << 16);
         }
-        rk[k / 2] = r0 | (r1 << 16);
+    } else {
+#pragma unroll
+        for (int k = 0; k < IPT; k += 2) {
+            uint32_t r0 = 0, r1 = 0;
+            if (one_digit) {
+                r0 = take_slot(s_cnt, digit_at<BYTE>(key[k], a.shift, a.mask), lane, true);
+                r1 = take_slot(s_cnt, digit_at<BYTE>(key[k + 1], a.shift, a.mask), lane, true);
+            } else {
+                if (k * T + tid < tile_n) r0 = atomicAdd(&s_cnt[digit_at<BYTE>(key[k], a.shift, a.mask)], 1u);
+                if ((k + 1) * T + tid < tile_n)
+                    r1 = atomicAdd(&s_cnt[digit_at<BYTE>(key[k + 1], a.shift, a.mask)], 1u);
+            }
+            rk[k / 2] = r0 | (r1 << 16);
+        }
     }
     __syncthreads();
 
@@ -948,24 +991,42 @@ struct FreePassConfig {
 
 // ------------------------------------------------------ bin starts
 // After the histogram ([CUDA3] kernel 2; [PMPP10] 10.3): the exclusive scan of
-// every pass's 256 counts, so that no tile scans them again, and (keys-only
-// sorts over every bit) the first pass's bin cursors set to its bin starts.
-// One CTA of 256 threads, one digit each.
+// every pass's 256 counts, so that no tile scans them again, (keys-only sorts
+// over every bit) the first pass's bin cursors set to its bin starts, and each
+// pass's most frequent digit where it is skewed.  One CTA of 256 threads, one
+// digit each.
 __global__ void __launch_bounds__(256) k_bin_starts(const uint32_t *__restrict__ hist, int passes,
-                                                    uint32_t *__restrict__ start,
-                                                    uint32_t *__restrict__ cursor) {
+                                                    uint32_t n_keys, uint32_t *__restrict__ start,
+                                                    uint32_t *__restrict__ cursor,
+                                                    uint32_t *__restrict__ hot) {
     __shared__ uint32_t s_sum[8];
+    __shared__ unsigned long long s_top[8];
     const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int p = 0; p < passes; ++p) {
         const uint32_t h = hist[p * 256 + tid];
         const uint32_t inc = warp_inclusive_scan(h, lane);
+        // (count, digit) of the largest bin; ties go to the lower digit
+        unsigned long long top = (static_cast<unsigned long long>(h) << 32) | (255u - tid);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const unsigned long long other = __shfl_xor_sync(kFullMask, top, o);
+            top = other > top ? other : top;
+        }
         if (lane == 31) s_sum[warp] = inc;
+        if (lane == 0) s_top[warp] = top;
         __syncthreads();
         uint32_t base = 0;
         for (uint32_t w = 0; w < warp; ++w) base += s_sum[w];
         const uint32_t st = base + inc - h;
         start[p * 256 + tid] = st;
         if (p == 0 && cursor != nullptr) cursor[tid] = st;
+        if (tid == 0) {
+            unsigned long long t = s_top[0];
+            for (int w = 1; w < 8; ++w) t = s_top[w] > t ? s_top[w] : t;
+            // skewed only when one digit holds more than 1/8 of the keys
+            // (32x its share among 256 equally likely digits); 256: none
+            hot[p] = static_cast<uint32_t>(t >> 32) > n_keys / 8u ? 255u - static_cast<uint32_t>(t & 0xFFu) : 256u;
+        }
         __syncthreads();
     }
 }

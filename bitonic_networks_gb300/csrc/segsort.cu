@@ -209,6 +209,7 @@ k_seg_pass(const PassArgs a, const SegTile *tiles, const uint32_t *counts, const
             s_misc[0] = atomicAdd(a.tile_counter, 1u);
             s_misc[1] = ld_relaxed(a.abort_flag);
             s_misc[2] = 0;
+            s_misc[3] = 256u;   // no skewed digit
         }
         for (uint32_t i = tid; i < kSegPassWarps * kRow; i += T) s_cnt[i] = 0;
         __syncthreads();

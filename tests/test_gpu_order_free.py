@@ -39,6 +39,11 @@ def keys32(shape: str, n: int, seed: int) -> np.ndarray:
         return (u & np.uint32(0xFFFF0000)) | ((w % np.uint32(3000)) * np.uint32(17))
     if shape == "top_only":    # only the top byte varies: passes 0-2 see equal digits
         return (u & np.uint32(0xFF000000)) | np.uint32(0x00ABCDEF)
+    if shape == "skewed_low":  # low byte 0 for 98 % of keys: pass 2 sees one long run, then
+        # runs of ~160 keys, so warps there straddle three or more runs (stable ranks after
+        # 16-byte loads of a pass whose runs are long on average)
+        lo = np.where(w % np.uint32(50) == 0, (w >> np.uint32(8)) % np.uint32(255) + np.uint32(1), 0)
+        return (u & np.uint32(0xFFFFFF00)) | lo.astype(np.uint32)
     if shape == "uniform":
         return u
     if shape == "and3":
@@ -52,7 +57,8 @@ def keys32(shape: str, n: int, seed: int) -> np.ndarray:
     raise ValueError(shape)
 
 
-SHAPES = ["low3", "mid_groups", "top_only", "uniform", "and3", "distinct16", "sorted", "reversed"]
+SHAPES = ["low3", "mid_groups", "top_only", "skewed_low", "uniform", "and3", "distinct16", "sorted",
+          "reversed"]
 
 
 @pytest.mark.parametrize("shape", SHAPES)
@@ -83,13 +89,18 @@ def test_mapped_32bit_keys(kind, desc, shape):
 
 @pytest.mark.parametrize("kind", [3, 4, 5])
 @pytest.mark.parametrize("desc", [False, True])
-@pytest.mark.parametrize("shape", ["low_runs", "uniform"])
+@pytest.mark.parametrize("shape", ["low_runs", "skewed_low", "uniform"])
 def test_64bit_keys(kind, desc, shape):
     n = (1 << 20) + 777
     base = synth.keys64(n, 7500 + kind)
     if shape == "low_runs":
         # the low 40 bits take 5 values, so the first five passes see long runs
         base = (base & np.uint64(0xFFFFFF0000000000)) | (base % np.uint64(5))
+    if shape == "skewed_low":
+        # low byte 0 for 98 % of keys: warps of pass 2 straddle many short runs
+        w = synth.keys64(n, 7600 + kind)
+        lo = np.where(w % np.uint64(50) == 0, (w >> np.uint64(8)) % np.uint64(255) + np.uint64(1), 0)
+        base = (base & np.uint64(0xFFFFFFFFFFFFFF00)) | lo.astype(np.uint64)
     if kind == 4:
         base = base & np.uint64(0xBFFFFFFFFFFFFFFF)   # finite doubles
     dt = {3: np.uint64, 4: np.float64, 5: np.int64}[kind]
