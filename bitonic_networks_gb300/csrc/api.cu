@@ -200,7 +200,9 @@ const char *gsort_status_string(int status) {
         case GSORT_EINVAL: return "GSORT_EINVAL: invalid argument";
         case GSORT_EALIGN: return "GSORT_EALIGN: misaligned pointer";
         case GSORT_EWORKSPACE: return "GSORT_EWORKSPACE: workspace missing or too small";
-        case GSORT_ETOOBIG: return "GSORT_ETOOBIG: n exceeds GSORT_MAX_N";
+        case GSORT_ETOOBIG:
+            return "GSORT_ETOOBIG: n (or the segment count) exceeds the entry point's maximum (GSORT_MAX_N; "
+                   "GSORT_COMPACT_NOALLOC_MAX_N for the allocation-free compaction)";
         case GSORT_ECUDA: return "GSORT_ECUDA: CUDA error";
         case GSORT_ETIMEOUT: return "GSORT_ETIMEOUT: a device-side look-back wait gave up";
         default: return "unknown gsort status";

@@ -51,7 +51,7 @@ typedef enum gsort_status {
     GSORT_EINVAL = -1,      /* bad argument: NULL, bad range, overlapping buffers */
     GSORT_EALIGN = -2,      /* a pointer is not 4-byte (data) or 256-byte (workspace) aligned */
     GSORT_EWORKSPACE = -3,  /* workspace missing or smaller than the *_workspace_bytes() answer */
-    GSORT_ETOOBIG = -4,     /* n > GSORT_MAX_N */
+    GSORT_ETOOBIG = -4,     /* n above the entry point's maximum (GSORT_MAX_N, or the smaller limit it states) */
     GSORT_ECUDA = -5,       /* a CUDA runtime call or kernel launch failed */
     GSORT_ETIMEOUT = -6     /* a device-side look-back wait gave up (see gsort_check) */
 } gsort_status;
