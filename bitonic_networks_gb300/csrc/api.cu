@@ -547,6 +547,8 @@ int gsort_radix_launch_count(int64_t n, int begin_bit, int end_bit, int in_place
 int gsort_radix_sort_launch_count(int64_t n, int kind, int begin_bit, int end_bit, int in_place) {
     const int kb = key_kind_bytes(kind);
     if (n <= 0 || begin_bit >= end_bit || kb == 0) return 0;
+    if (kb == 4 && n <= 65536)
+        return 1;   // one cluster kernel for every pass (where such a cluster fits the device)
     if (n <= GSORT_MAX_N && small_sort_applies(static_cast<uint32_t>(n), kb, 0))
         return 2;   // header clear + one cooperative kernel for every pass
     const int passes = (end_bit - begin_bit + 7) / 8;

@@ -269,6 +269,14 @@ bool small_sort_applies(uint32_t n, int key_bytes, int variant);
 uint32_t small_sort_tile();
 int launch_small_sort(const SmallSortLaunch &L);
 
+// Inputs of at most 65,536 32-bit keys (cluster_sort.cu): every pass inside
+// one thread-block cluster, keys resident in shared memory; no header clear.
+// launch_cluster_sort returns 1 (and launches nothing) when no cluster of its
+// shapes can be resident; counts, bar_count, spin_limit and stall_tile of the
+// launch description are not used.
+bool cluster_sort_applies(uint32_t n, int key_bytes, int variant, uint32_t stall_tile, int passes);
+int launch_cluster_sort(const SmallSortLaunch &L);
+
 // 2-way split (split.cu): partition by a predicate, and the 1-bit split sort.
 struct SplitLayout {
     uint32_t tiles;

@@ -318,7 +318,36 @@ int launch_radix(const RadixLaunch &L) {
     void *tmp_k = L.ws + lay.tmp_keys;
     uint32_t *tmp_v = pairs ? reinterpret_cast<uint32_t *>(L.ws + lay.tmp_vals) : nullptr;
 
+    const uint32_t last_width = static_cast<uint32_t>(L.end_bit - L.begin_bit - 8 * (passes - 1));
+    const uint32_t last_mask = (1u << last_width) - 1u;
+    const bool alias = (L.keys_in == L.keys_out) || (pairs && L.vals_in == L.vals_out);
+
     record(L.events, L.num_events, 0, s);
+    if (cluster_sort_applies(L.n, order.key_bytes, L.variant, L.stall_tile, passes)) {
+        // one launch, no header clear (the kernel clears the status words)
+        SmallSortLaunch S{};
+        S.keys_in = static_cast<const uint32_t *>(L.keys_in);
+        S.keys_out = static_cast<uint32_t *>(L.keys_out);
+        S.vals_in = L.vals_in;
+        S.vals_out = L.vals_out;
+        S.n = L.n;
+        S.passes = passes;
+        S.begin_bit = L.begin_bit;
+        S.last_mask = last_mask;
+        S.fmask = static_cast<uint32_t>(order.fmask);
+        S.flip = static_cast<uint32_t>(order.flip);
+        S.alias = alias;
+        S.status = status;
+        S.abort_flag = abort_flag;
+        S.stream = s;
+        S.sm_count = L.sm_count;
+        record(L.events, L.num_events, 1, s);
+        const int rc = launch_cluster_sort(S);
+        if (rc != 1) {
+            for (int i = 2; i < 3 + passes; ++i) record(L.events, L.num_events, i, s);
+            return rc;
+        }
+    }
     k_zero_words<<<1, 256, 0, s>>>(hdr, static_cast<uint32_t>(kHdrBytes / sizeof(uint32_t)));
     if (cudaGetLastError() != cudaSuccess) return GSORT_ECUDA;
     if (kb == 8) {
@@ -326,10 +355,6 @@ int launch_radix(const RadixLaunch &L) {
         if (cudaGetLastError() != cudaSuccess) return GSORT_ECUDA;
     }
     record(L.events, L.num_events, 1, s);
-
-    const uint32_t last_width = static_cast<uint32_t>(L.end_bit - L.begin_bit - 8 * (passes - 1));
-    const uint32_t last_mask = (1u << last_width) - 1u;
-    const bool alias = (L.keys_in == L.keys_out) || (pairs && L.vals_in == L.vals_out);
 
     if (small_sort_applies(L.n, order.key_bytes, L.variant)) {
         SmallSortLaunch S;

@@ -172,7 +172,9 @@ def test_partition_and_split_sort_argument_errors(lib):
 
 
 def test_launch_count(lib):
-    assert lib.gsort_radix_launch_count(100, 0, 32, 0) == 2          # small input: one cooperative kernel
+    assert lib.gsort_radix_launch_count(100, 0, 32, 0) == 1          # up to 65,536 keys: one cluster kernel
+    assert lib.gsort_radix_launch_count(1 << 16, 0, 32, 0) == 1
+    assert lib.gsort_radix_launch_count((1 << 16) + 1, 0, 32, 0) == 2  # then one cooperative kernel
     assert lib.gsort_radix_launch_count(1 << 18, 0, 32, 1) == 2
     # header clear, histogram, bin starts, the passes
     assert lib.gsort_radix_launch_count((1 << 18) + 1, 0, 32, 0) == 7
@@ -183,7 +185,7 @@ def test_launch_count(lib):
     assert lib.gsort_radix_sort_launch_count(100, 3, 0, 64, 0) == 12      # 3 + 8 passes + hist clear
     assert lib.gsort_radix_sort_launch_count(100, 5, 0, 56, 1) == 12      # 7 passes, in place: + copy
     assert lib.gsort_radix_sort_launch_count(1 << 20, 2, 0, 32, 0) == 7
-    assert lib.gsort_radix_sort_launch_count(100, 2, 0, 32, 0) == 2
+    assert lib.gsort_radix_sort_launch_count(100, 2, 0, 32, 0) == 1
 
 
 # Fake device addresses: validation rejects these calls before any CUDA call.
