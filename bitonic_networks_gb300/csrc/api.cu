@@ -552,9 +552,9 @@ int gsort_radix_sort_launch_count(int64_t n, int kind, int begin_bit, int end_bi
     if (n <= GSORT_MAX_N && small_sort_applies(static_cast<uint32_t>(n), kb, 0))
         return 2;   // header clear + one cooperative kernel for every pass
     const int passes = (end_bit - begin_bit + 7) / 8;
-    // header clear, histogram, bin starts, the passes [, the copy back of an
-    // odd pass count in place] [, the 64-bit histogram clear]
-    return 3 + passes + ((in_place && (passes & 1)) ? 1 : 0) + (kb == 8 ? 1 : 0);
+    // header clear, histogram, the passes [, the copy back of an odd pass
+    // count in place] [, the 64-bit histogram clear]
+    return 2 + passes + ((in_place && (passes & 1)) ? 1 : 0) + (kb == 8 ? 1 : 0);
 }
 
 }  // extern "C"

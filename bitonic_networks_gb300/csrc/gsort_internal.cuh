@@ -18,6 +18,7 @@ constexpr size_t kHdrAbort = 4;       // u32: non-zero once a wait gave up; late
 constexpr size_t kHdrCounters = 128;  // u32 tile counters, one per 128-byte line
 constexpr int kNumCounters = 8;
 constexpr size_t kHdrKept = kHdrCounters + 128 * kNumCounters;  // u64 kept count (compaction)
+constexpr size_t kHdrHistDone = kHdrKept + 128;   // u32 finished CTAs of the histogram kernel (radix)
 constexpr size_t kHdrHist = 2048;     // u32[4][256] digit histograms (radix, 32-bit keys)
 constexpr size_t kHdrCursor = kHdrHist + 4096;   // u32[256] bin cursors of an order-free first pass (radix)
 constexpr size_t kHdrHot = kHdrCursor + 1024;    // u32[8] most frequent digit of each pass (radix)

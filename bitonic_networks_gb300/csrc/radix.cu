@@ -280,15 +280,16 @@ namespace {
 
 cudaError_t launch_hist_any(const void *keys, uint32_t n, const KeyOrder &o, int begin_bit,
                             int passes, uint32_t last_mask, uint32_t *hist, uint32_t *clear,
-                            uint32_t clear_words, cudaStream_t s, int sm_count) {
+                            uint32_t clear_words, cudaStream_t s, int sm_count,
+                            const BinStartsOut &bs = BinStartsOut()) {
     const bool xf = o.fmask != 0 || o.flip != 0;
     if (o.key_bytes == 8)
         return launch_hist_u64(static_cast<const uint64_t *>(keys), n, xf, o.fmask, o.flip, begin_bit,
-                               passes, last_mask, hist, clear, clear_words, s, sm_count);
+                               passes, last_mask, hist, clear, clear_words, s, sm_count, bs);
     return launch_hist_kernel<uint32_t>(static_cast<const uint32_t *>(keys), n, xf,
                                         static_cast<uint32_t>(o.fmask), static_cast<uint32_t>(o.flip),
                                         begin_bit, passes, last_mask, hist, clear, clear_words, s,
-                                        sm_count);
+                                        sm_count, bs);
 }
 
 }  // namespace
@@ -386,16 +387,21 @@ int launch_radix(const RadixLaunch &L) {
         }
     }
 
-    // the histogram kernel also clears the first pass's look-back words
-    if (launch_hist_any(L.keys_in, L.n, order, L.begin_bit, passes, last_mask, hist, look[0],
-                        tiles * 256, s, L.sm_count) != cudaSuccess)
-        return GSORT_ECUDA;
     // keys only, every bit: equal keys are indistinguishable, so a warp needs
     // stable ranks only where its keys differ below the current digit
     const bool order_free = !pairs && L.begin_bit == 0 && L.end_bit == static_cast<int>(8 * kb);
     uint32_t *hot = reinterpret_cast<uint32_t *>(L.ws + kHdrHot);
-    k_bin_starts<<<1, 256, 0, s>>>(hist, passes, L.n, starts, order_free ? cursor : nullptr, hot);
-    if (cudaGetLastError() != cudaSuccess) return GSORT_ECUDA;
+    // the histogram kernel also clears the first pass's look-back words, and
+    // its last CTA writes the bin starts, the first pass's cursors and the
+    // skewed digits
+    BinStartsOut bs;
+    bs.start = starts;
+    bs.cursor = order_free ? cursor : nullptr;
+    bs.hot = hot;
+    bs.done = reinterpret_cast<uint32_t *>(L.ws + kHdrHistDone);
+    if (launch_hist_any(L.keys_in, L.n, order, L.begin_bit, passes, last_mask, hist, look[0],
+                        tiles * 256, s, L.sm_count, bs) != cudaSuccess)
+        return GSORT_ECUDA;
     record(L.events, L.num_events, 2, s);
 
     // In place (either array): in -> tmp -> out -> tmp ...; an odd pass count

@@ -29,9 +29,10 @@ uint32_t pass_tile_u64() { return Config64::kTile; }
 
 cudaError_t launch_hist_u64(const uint64_t *keys, uint32_t n, bool xf, uint64_t fmask, uint64_t flip,
                             int begin_bit, int passes, uint32_t last_mask, uint32_t *hist,
-                            uint32_t *clear, uint32_t clear_words, cudaStream_t s, int sm_count) {
+                            uint32_t *clear, uint32_t clear_words, cudaStream_t s, int sm_count,
+                            const BinStartsOut &bs) {
     return launch_hist_kernel<uint64_t>(keys, n, xf, fmask, flip, begin_bit, passes, last_mask, hist,
-                                        clear, clear_words, s, sm_count);
+                                        clear, clear_words, s, sm_count, bs);
 }
 
 }  // namespace gsort

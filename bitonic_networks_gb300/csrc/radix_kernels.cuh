@@ -94,16 +94,27 @@ struct PassArgs {
     // tile by block index.
     uint32_t *cursor = nullptr;
     // Non-null: the bin starts of this pass (the exclusive scan of `hist`,
-    // written by k_bin_starts), so that no tile scans the 256 counts again.
+    // written by the histogram kernel), so that no tile scans the 256 counts again.
     const uint32_t *start = nullptr;
     // Non-null: the pass's most frequent digit if it holds more than 1/8 of
-    // the keys, else 256 (written by k_bin_starts).
+    // the keys, else 256 (written by the histogram kernel).
     const uint32_t *hot = nullptr;
 };
 
 // Launch of one digit pass over `tiles` tiles (one configuration of the kernel).
 using PassLauncher = cudaError_t (*)(const PassArgs &, bool pairs, bool xin, bool xout,
                                      uint32_t tiles, cudaStream_t);
+
+// Where the histogram kernel's last CTA writes what the passes need from the
+// finished histogram (all null: nothing): the bin starts of every pass, the
+// first pass's bin cursors set to its bin starts (null: none), each pass's
+// skewed digit (256: none), and a zeroed counter of finished CTAs.
+struct BinStartsOut {
+    uint32_t *start = nullptr;
+    uint32_t *cursor = nullptr;
+    uint32_t *hot = nullptr;
+    uint32_t *done = nullptr;
+};
 
 // 64-bit keys (radix64.cu): the digit pass, its tile size, and the histogram.
 cudaError_t launch_pass_u64(const PassArgs &a, bool pairs, bool xin, bool xout, uint32_t tiles,
@@ -113,7 +124,8 @@ cudaError_t launch_pass_u64_free(const PassArgs &a, bool pairs, bool xin, bool x
 uint32_t pass_tile_u64();
 cudaError_t launch_hist_u64(const uint64_t *keys, uint32_t n, bool xf, uint64_t fmask, uint64_t flip,
                             int begin_bit, int passes, uint32_t last_mask, uint32_t *hist,
-                            uint32_t *clear, uint32_t clear_words, cudaStream_t s, int sm_count);
+                            uint32_t *clear, uint32_t clear_words, cudaStream_t s, int sm_count,
+                            const BinStartsOut &bs);
 
 namespace {
 
@@ -206,11 +218,61 @@ __device__ __forceinline__ void hist_count(uint32_t *col, uint64_t k, uint32_t b
     }
 }
 
+// The finished histogram's bin starts ([CUDA3] kernel 2; [PMPP10] 10.3), the
+// first pass's bin cursors and each pass's skewed digit, computed by the
+// histogram kernel's last CTA (kHistThreads threads: four passes at a time,
+// 256 threads per pass, one digit each).  `scratch` holds 64 words.
+__device__ __forceinline__ void bin_starts_block(const uint32_t *hist, int passes, uint32_t n,
+                                                 const BinStartsOut &bs, uint32_t *scratch) {
+    const uint32_t tid = threadIdx.x, lane = tid & 31, g = tid >> 8, wg = (tid >> 5) & 7, d = tid & 255;
+    uint32_t *s_sum = scratch;        // [4][8]
+    uint32_t *s_top = scratch + 32;   // [4][8]: (count << 8 | 255 - digit) of each warp's largest bin
+    for (int p0 = 0; p0 < passes; p0 += 4) {
+        const int p = p0 + static_cast<int>(g);
+        const uint32_t h = p < passes ? __ldcg(hist + p * 256 + d) : 0u;
+        const uint32_t inc = warp_inclusive_scan(h, lane);
+        // the largest count first (a bin may hold every key, so no digit fits
+        // beside it in one word), then the lowest digit holding it
+        uint32_t m = h;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(kFullMask, m, o));
+        if (lane == 31) s_sum[g * 8 + wg] = inc;
+        if (lane == 0) s_top[g * 8 + wg] = m;
+        __syncthreads();
+        uint32_t base = 0, top = 0;
+        for (uint32_t w = 0; w < 8; ++w) {
+            if (w < wg) base += s_sum[g * 8 + w];
+            top = max(top, s_top[g * 8 + w]);
+        }
+        __syncthreads();
+        if (p < passes) {
+            const uint32_t st = base + inc - h;
+            bs.start[p * 256 + d] = st;
+            if (p == 0 && bs.cursor != nullptr) bs.cursor[d] = st;
+            // skewed only when one digit holds more than 1/8 of the keys (32x its
+            // share among 256 equally likely digits); the lowest such digit
+            if (top > n / 8u) {
+                const uint32_t firsts = __ballot_sync(kFullMask, h == top);
+                if (lane == 0) s_top[g * 8 + wg] = firsts ? wg * 32 + __ffs(firsts) - 1 : 256u;
+            } else if (lane == 0) {
+                s_top[g * 8 + wg] = 256u;
+            }
+        }
+        __syncthreads();
+        if (p < passes && d == 0) {
+            uint32_t hd = 256u;
+            for (uint32_t w = 0; w < 8; ++w) hd = min(hd, s_top[g * 8 + w]);
+            bs.hot[p] = hd;
+        }
+        __syncthreads();
+    }
+}
+
 template <class K, bool XF, bool BYTE>
 __global__ void __launch_bounds__(kHistThreads, 1)
 k_digit_hist(const K *__restrict__ keys, uint32_t n, uint32_t begin_bit, int passes,
              uint32_t last_mask, K fmask, K flip, uint32_t *__restrict__ hist,
-             uint4 *__restrict__ clear, uint32_t clear_vec4) {
+             uint4 *__restrict__ clear, uint32_t clear_vec4, const BinStartsOut bs) {
     constexpr bool kWide = sizeof(K) == 8;
     constexpr uint32_t kPerVec = 16 / sizeof(K);   // keys per 16-byte load
     extern __shared__ uint32_t s_h[];
@@ -272,6 +334,17 @@ k_digit_hist(const K *__restrict__ keys, uint32_t n, uint32_t begin_bit, int pas
         }
         if (s) atomicAdd(&hist[i], s);
     }
+    if (bs.done == nullptr) return;
+    // the last CTA to finish finds the histogram complete: every CTA's adds
+    // are ordered before its count of finished CTAs by the fence
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_h[0] = atomicAdd(bs.done, 1u) == gridDim.x - 1 ? 1u : 0u;
+    __syncthreads();
+    if (s_h[0] == 0u) return;
+    __threadfence();
+    __syncthreads();
+    bin_starts_block(hist, passes, n, bs, s_h + 32);
 }
 
 // ------------------------------------------------------- warp multisplit
@@ -989,54 +1062,13 @@ struct FreePassConfig {
     }
 };
 
-// ------------------------------------------------------ bin starts
-// After the histogram ([CUDA3] kernel 2; [PMPP10] 10.3): the exclusive scan of
-// every pass's 256 counts, so that no tile scans them again, (keys-only sorts
-// over every bit) the first pass's bin cursors set to its bin starts, and each
-// pass's most frequent digit where it is skewed.  One CTA of 256 threads, one
-// digit each.
-__global__ void __launch_bounds__(256) k_bin_starts(const uint32_t *__restrict__ hist, int passes,
-                                                    uint32_t n_keys, uint32_t *__restrict__ start,
-                                                    uint32_t *__restrict__ cursor,
-                                                    uint32_t *__restrict__ hot) {
-    __shared__ uint32_t s_sum[8];
-    __shared__ unsigned long long s_top[8];
-    const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int p = 0; p < passes; ++p) {
-        const uint32_t h = hist[p * 256 + tid];
-        const uint32_t inc = warp_inclusive_scan(h, lane);
-        // (count, digit) of the largest bin; ties go to the lower digit
-        unsigned long long top = (static_cast<unsigned long long>(h) << 32) | (255u - tid);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const unsigned long long other = __shfl_xor_sync(kFullMask, top, o);
-            top = other > top ? other : top;
-        }
-        if (lane == 31) s_sum[warp] = inc;
-        if (lane == 0) s_top[warp] = top;
-        __syncthreads();
-        uint32_t base = 0;
-        for (uint32_t w = 0; w < warp; ++w) base += s_sum[w];
-        const uint32_t st = base + inc - h;
-        start[p * 256 + tid] = st;
-        if (p == 0 && cursor != nullptr) cursor[tid] = st;
-        if (tid == 0) {
-            unsigned long long t = s_top[0];
-            for (int w = 1; w < 8; ++w) t = s_top[w] > t ? s_top[w] : t;
-            // skewed only when one digit holds more than 1/8 of the keys
-            // (32x its share among 256 equally likely digits); 256: none
-            hot[p] = static_cast<uint32_t>(t >> 32) > n_keys / 8u ? 255u - static_cast<uint32_t>(t & 0xFFu) : 256u;
-        }
-        __syncthreads();
-    }
-}
-
 // Histogram launch: one CTA per SM (fewer for small inputs: about 16 keys per
 // thread at least).
 template <class K>
 cudaError_t launch_hist_kernel(const K *keys, uint32_t n, bool xf, K fmask, K flip, int begin_bit,
                                int passes, uint32_t last_mask, uint32_t *hist, uint32_t *clear,
-                               uint32_t clear_words, cudaStream_t s, int sm_count) {
+                               uint32_t clear_words, cudaStream_t s, int sm_count,
+                               const BinStartsOut &bs = BinStartsOut()) {
     const uint32_t want = (n + kHistThreads * 16 - 1) / (kHistThreads * 16);
     const uint32_t grid = std::max(1u, std::min(want, static_cast<uint32_t>(sm_count)));
     uint4 *cl = reinterpret_cast<uint4 *>(clear);
@@ -1047,7 +1079,7 @@ cudaError_t launch_hist_kernel(const K *keys, uint32_t n, bool xf, K fmask, K fl
     cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(k), kHistSmemBytes);
     if (e != cudaSuccess) return e;
     k<<<grid, kHistThreads, smem, s>>>(keys, n, begin_bit, passes, last_mask, fmask, flip, hist, cl,
-                                       clear_words / 4);
+                                       clear_words / 4, bs);
     return cudaGetLastError();
 }
 

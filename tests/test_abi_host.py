@@ -176,15 +176,15 @@ def test_launch_count(lib):
     assert lib.gsort_radix_launch_count(1 << 16, 0, 32, 0) == 1
     assert lib.gsort_radix_launch_count((1 << 16) + 1, 0, 32, 0) == 2  # then one cooperative kernel
     assert lib.gsort_radix_launch_count(1 << 18, 0, 32, 1) == 2
-    # header clear, histogram, bin starts, the passes
-    assert lib.gsort_radix_launch_count((1 << 18) + 1, 0, 32, 0) == 7
-    assert lib.gsort_radix_launch_count(1 << 20, 0, 8, 0) == 4
-    assert lib.gsort_radix_launch_count(1 << 20, 0, 24, 1) == 7
+    # header clear, histogram (its last CTA writes the bin starts), the passes
+    assert lib.gsort_radix_launch_count((1 << 18) + 1, 0, 32, 0) == 6
+    assert lib.gsort_radix_launch_count(1 << 20, 0, 8, 0) == 3
+    assert lib.gsort_radix_launch_count(1 << 20, 0, 24, 1) == 6
     assert lib.gsort_radix_launch_count(0, 0, 32, 0) == 0
     assert lib.gsort_radix_launch_count(100, 5, 5, 0) == 0
-    assert lib.gsort_radix_sort_launch_count(100, 3, 0, 64, 0) == 12      # 3 + 8 passes + hist clear
-    assert lib.gsort_radix_sort_launch_count(100, 5, 0, 56, 1) == 12      # 7 passes, in place: + copy
-    assert lib.gsort_radix_sort_launch_count(1 << 20, 2, 0, 32, 0) == 7
+    assert lib.gsort_radix_sort_launch_count(100, 3, 0, 64, 0) == 11      # 2 + 8 passes + hist clear
+    assert lib.gsort_radix_sort_launch_count(100, 5, 0, 56, 1) == 11      # 7 passes, in place: + copy
+    assert lib.gsort_radix_sort_launch_count(1 << 20, 2, 0, 32, 0) == 6
     assert lib.gsort_radix_sort_launch_count(100, 2, 0, 32, 0) == 1
 
 
