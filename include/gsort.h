@@ -350,8 +350,10 @@ int gsort_radix_sort_ex(const void *d_keys_in, void *d_keys_out,
                         const gsort_options *options);
 
 /* Events for the segmented sort: [0] start, [1] after the classification,
- * [2] after the small segments, [3] after the large segments' histograms,
- * [4 + p] after digit pass p of the large segments. */
+ * [3] after the large segments' histograms, [4 + p] after digit pass p of
+ * the large segments, [2] at the end, once the small segments are sorted too
+ * (their networks run on streams of the library's own beside the large
+ * segments' kernels; `stream` waits for them before [2]). */
 int gsort_segmented_sort_ex(const void *d_keys_in, void *d_keys_out,
                             const uint32_t *d_vals_in, uint32_t *d_vals_out, int64_t n,
                             const uint32_t *d_offsets, int64_t num_segments,

@@ -7,7 +7,8 @@ OP: keys (uint32 keys, 32 bits), pairs (uint32 key/index pairs), fpairs
 (float keys with index values), compact (compaction input), segments (1024-key
 segments, n/1024 of them), hist (the digit-histogram step alone), sort (any
 key kind: --kind u32|f32|i32|u64|f64|i64 [--desc] [--values]), segsort
-(variable-length segments, --mix small|mixed|large [--values] [--desc]),
+(variable-length segments, --mix small|mixed|large [--dist uniform|and3|distinct16]
+[--values] [--desc]),
 partition (compaction input split by x > 0 [--values]), splitsort (the 1-bit
 split sort of uint32 keys [--values]).
 --time prints the median CUDA-event time of the timed calls.
@@ -33,6 +34,7 @@ def main(argv=None) -> int:
     ap.add_argument("op", choices=["keys", "pairs", "fpairs", "compact", "segments", "hist", "sort",
                                    "segsort", "partition", "splitsort"])
     ap.add_argument("--mix", choices=["small", "mixed", "large"], default="mixed")
+    ap.add_argument("--dist", choices=["uniform", "and3", "distinct16"], default="uniform")
     ap.add_argument("--kind", choices=["u32", "f32", "i32", "u64", "f64", "i64"], default="u64")
     ap.add_argument("--desc", action="store_true")
     ap.add_argument("--values", action="store_true")
@@ -58,7 +60,8 @@ def main(argv=None) -> int:
         x = up(synth.uniform_keys(n, 10))
         v = up(synth.index_values(n)) if a.values else None
     elif a.op == "segsort":
-        x = up(synth.uniform_keys(n, 7))
+        x = up({"uniform": synth.uniform_keys, "and3": synth.and3_keys,
+                "distinct16": synth.distinct16_keys}[a.dist](n, 7))
         off_np = synth.segment_offsets(n, a.mix, 8)
         off = up(off_np)
         v = up(synth.index_values(n)) if a.values else None

@@ -105,6 +105,7 @@ def test_heavy_duplicates_are_stable():
     keys = (synth.uniform_keys(n, 5) % np.uint32(7)).astype(np.uint32)   # 7 distinct keys
     for desc in (False, True):
         check(keys, lens, 0, desc, True)
+        check(keys, lens, 0, desc, False)   # keys only: one digit value per bin cursor
 
 
 def test_single_segment_large():
@@ -152,3 +153,58 @@ def test_bad_offsets_reported(bad):
     ok_off = offsets_of([n])
     ko, _ = gsort.segmented_sort(keys, to_dev(ok_off), None, kind=0)
     assert np.array_equal(host(ko), np.sort(host(keys)))
+
+
+def test_keys_not_16_byte_aligned():
+    """Keys that start 4 or 8 bytes past a 16-byte boundary (the histogram
+    takes its 16-byte loads only from aligned keys)."""
+    lens = [70_001, 3, 1025, 9000, 500, 20_000]
+    off = to_dev(offsets_of(lens))
+    n = sum(lens)
+    for shift in (1, 2):
+        keys = keys_for(0, n, 60 + shift)
+        buf = torch.zeros(n + 4, dtype=torch.int32, device="cuda")
+        kt = buf[shift:shift + n]
+        kt.copy_(to_dev(keys))
+        assert kt.data_ptr() % 16 == 4 * shift
+        ko, _ = gsort.segmented_sort(kt, off, kind=0)
+        ek, _ = oracle.default().segmented_sort_general(keys, offsets_of(lens), None, 0, False)
+        assert np.array_equal(host(ko), np.ascontiguousarray(ek).view(np.uint32)), f"shift {shift}"
+
+
+def test_concurrent_callers_on_their_own_streams():
+    """Two host threads sort at once, each on a stream of its own (the small
+    segments' networks of every call run on streams the library shares
+    between calls)."""
+    import threading
+
+    lens = mixed_lengths(31, 120_000, hi=20_000)
+    off_h = offsets_of(lens)
+    n = sum(lens)
+    keys = [keys_for(0, n, 90 + t) for t in range(2)]
+    expect = [np.ascontiguousarray(oracle.default().segmented_sort_general(k, off_h, None, 0, False)[0])
+              .view(np.uint32) for k in keys]
+    errors = []
+
+    def worker(t):
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                kt = to_dev(keys[t])
+                ot = to_dev(off_h)
+                for _ in range(20):
+                    ko, _ = gsort.segmented_sort(kt, ot, kind=0)
+                    got = ko.cpu().numpy().view(np.uint32)
+                    if not np.array_equal(got, expect[t]):
+                        errors.append(f"thread {t}: result differs")
+                        return
+        except Exception as e:   # reported below
+            errors.append(f"thread {t}: {e!r}")
+
+    th = [threading.Thread(target=worker, args=(t,)) for t in range(2)]
+    for x in th:
+        x.start()
+    for x in th:
+        x.join()
+    assert not errors, errors
+
