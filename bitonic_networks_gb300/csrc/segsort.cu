@@ -871,9 +871,13 @@ int launch_segmented_sort(const SegLaunch &L) {
     SideStreams *side = side_streams();
     if (side != nullptr && cudaEventRecord(side->fork, s) != cudaSuccess) return GSORT_ECUDA;
     const uint32_t sgrid = std::max(1u, std::min((lay.small_max + kSmallWarps - 1) / kSmallWarps, sms * 16));
-    for (int c = 0; c < kSmallClasses; ++c) {
+    int rc = GSORT_OK, forked = 0;   // side streams whose work the caller's stream must wait for
+    for (int c = 0; c < kSmallClasses && rc == GSORT_OK; ++c) {
         cudaStream_t ss = side != nullptr ? side->st[c] : s;
-        if (side != nullptr && cudaStreamWaitEvent(ss, side->fork, 0) != cudaSuccess) return GSORT_ECUDA;
+        if (side != nullptr && cudaStreamWaitEvent(ss, side->fork, 0) != cudaSuccess) {
+            rc = GSORT_ECUDA;
+            break;
+        }
         cudaError_t e;
         if (pairs)
             e = mapped ? launch_small<true, true>(c, L.offsets, small_list, counts, lay.small_max, L.keys_in,
@@ -888,13 +892,16 @@ int launch_segmented_sort(const SegLaunch &L) {
                        : launch_small<false, false>(c, L.offsets, small_list, counts, lay.small_max, L.keys_in,
                                                     L.keys_out, nullptr, nullptr, fmask, flip, abort_flag, sgrid,
                                                     ss);
-        if (e != cudaSuccess) return GSORT_ECUDA;
-        if (side != nullptr && cudaEventRecord(side->join[c], ss) != cudaSuccess) return GSORT_ECUDA;
+        if (side != nullptr) {
+            // joined even after a failed launch: whatever reached the side stream is waited for
+            if (cudaEventRecord(side->join[c], ss) == cudaSuccess) ++forked;
+            else rc = GSORT_ECUDA;
+        }
+        if (e != cudaSuccess) rc = GSORT_ECUDA;
     }
-    const int rc = launch_large_segments(L, lay, pairs, mapped, order, s);
-    if (side != nullptr)
-        for (int c = 0; c < kSmallClasses; ++c)
-            if (cudaStreamWaitEvent(s, side->join[c], 0) != cudaSuccess) return GSORT_ECUDA;
+    if (rc == GSORT_OK) rc = launch_large_segments(L, lay, pairs, mapped, order, s);
+    for (int c = 0; c < forked; ++c)
+        if (cudaStreamWaitEvent(s, side->join[c], 0) != cudaSuccess) rc = GSORT_ECUDA;
     record(L.events, L.num_events, 2, s);
     return rc;
 }
