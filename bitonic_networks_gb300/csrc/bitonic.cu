@@ -47,7 +47,7 @@ k_bitonic_segments(uint32_t *keys, uint32_t num_segments, uint32_t len) {
         x[r] = sw[e + (e >> 5)];
     }
 
-    bitonic_registers<LOG_R>(x, lane);
+    bitonic_registers<LOG_R>(x, lane, sw);
 
     __syncwarp();
 #pragma unroll

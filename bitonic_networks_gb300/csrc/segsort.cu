@@ -559,7 +559,7 @@ __device__ __forceinline__ void sort_small(const uint32_t *keys_in, uint32_t *ke
         const uint32_t e = lane * R + r;
         x[r] = sw[e + (e >> 5)];
     }
-    bitonic_registers<LOG_R>(x, lane);
+    bitonic_registers<LOG_R>(x, lane, sw);
     __syncwarp();
 #pragma unroll
     for (int r = 0; r < R; ++r) {
