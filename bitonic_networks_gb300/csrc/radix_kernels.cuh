@@ -960,15 +960,29 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass_free(const Pass
         one_digit = __all_sync(kFullMask, same);
     }
     uint32_t rk[IPT / 2];
+    uint32_t hot_base = 0;
     if (hot < 256u && !one_digit) {   // the same in every thread of the grid
+        // keys of the hot digit rank by this warp's running count of them, and
+        // the warp reserves their slots with one atomic after the loop (their
+        // order is free); bit 15 marks such a rank until then
+        const uint32_t ltm = lanemask_lt();
+        uint32_t run = 0;
 #pragma unroll
         for (int k = 0; k < IPT; k += 2) {
-            const uint32_t r0 = take_slot_hot(s_cnt, digit_at<BYTE>(key[k], a.shift, a.mask), hot, lane,
-                                              k * T + tid < tile_n);
-            const uint32_t r1 = take_slot_hot(s_cnt, digit_at<BYTE>(key[k + 1], a.shift, a.mask), hot, lane,
-                                              (k + 1) * T + tid < tile_n);
-            rk[k / 2] = r0 | (r1 << 16);
+            uint32_t r[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const bool valid = (k + u) * T + tid < tile_n;
+                const uint32_t d = digit_at<BYTE>(key[k + u], a.shift, a.mask);
+                const bool h = valid && d == hot;
+                const uint32_t hm = __ballot_sync(kFullMask, h);
+                r[u] = h ? (0x8000u | (run + __popc(hm & ltm))) : (valid ? atomicAdd(&s_cnt[d], 1u) : 0u);
+                run += __popc(hm);
+            }
+            rk[k / 2] = r[0] | (r[1] << 16);
         }
+        if (lane == 0 && run != 0) hot_base = atomicAdd(&s_cnt[hot], run);
+        hot_base = __shfl_sync(kFullMask, hot_base, 0);
     } else {
 #pragma unroll
         for (int k = 0; k < IPT; k += 2) {
@@ -1006,11 +1020,22 @@ __global__ void __launch_bounds__(WARPS * 32, MINB) k_digit_pass_free(const Pass
     if (tid < 256 && cnt != 0 && tile != a.stall_tile) excl = atomicAdd(a.cursor + tid, cnt);
     if (a.look_clear != nullptr)
         for (uint32_t i = tid; i < 256; i += T) a.look_clear[tile * 256 + i] = 0;
+    if (hot < 256u && !one_digit) {
 #pragma unroll
-    for (int k = 0; k < IPT; ++k) {
-        if (k * T + tid < tile_n) {
-            const uint32_t r = (rk[k / 2] >> ((k & 1) * 16)) & 0xFFFFu;
-            s_keys[s_cnt[digit_at<BYTE>(key[k], a.shift, a.mask)] + r] = key[k];
+        for (int k = 0; k < IPT; ++k) {
+            if (k * T + tid < tile_n) {
+                uint32_t r = (rk[k / 2] >> ((k & 1) * 16)) & 0xFFFFu;
+                if (r & 0x8000u) r = hot_base + (r & 0x7FFFu);
+                s_keys[s_cnt[digit_at<BYTE>(key[k], a.shift, a.mask)] + r] = key[k];
+            }
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < IPT; ++k) {
+            if (k * T + tid < tile_n) {
+                const uint32_t r = (rk[k / 2] >> ((k & 1) * 16)) & 0xFFFFu;
+                s_keys[s_cnt[digit_at<BYTE>(key[k], a.shift, a.mask)] + r] = key[k];
+            }
         }
     }
     if (tid < 256) s_goff[tid] = excl - tile_excl;   // the cursor started at the bin's start

@@ -7,10 +7,10 @@ OP: keys (uint32 keys, 32 bits), pairs (uint32 key/index pairs), fpairs
 (float keys with index values), compact (compaction input), segments (1024-key
 segments, n/1024 of them), hist (the digit-histogram step alone), sort (any
 key kind: --kind u32|f32|i32|u64|f64|i64 [--desc] [--values]), segsort
-(variable-length segments, --mix small|mixed|large [--dist uniform|and3|distinct16]
-[--values] [--desc]),
+(variable-length segments, --mix small|mixed|large [--values] [--desc]),
 partition (compaction input split by x > 0 [--values]), splitsort (the 1-bit
 split sort of uint32 keys [--values]).
+keys, hist and segsort take --dist uniform|and3|distinct16 (the key distribution).
 --time prints the median CUDA-event time of the timed calls.
 Each call is followed by a device-status check; the process exits non-zero on
 any error, so a profiler only ever runs a command that finished cleanly.
@@ -74,7 +74,8 @@ def main(argv=None) -> int:
         x = torch.from_numpy(np.ascontiguousarray(kx)).to(dev)
         v = up(synth.index_values(n)) if a.values else None
     elif a.op in ("keys", "hist"):
-        x = up(synth.uniform_keys(n, 1))
+        x = up({"uniform": synth.uniform_keys, "and3": synth.and3_keys,
+                "distinct16": synth.distinct16_keys}[a.dist](n, 1))
     elif a.op == "pairs":
         x, v = up(synth.uniform_keys(n, 2)), up(synth.index_values(n))
     elif a.op == "fpairs":
