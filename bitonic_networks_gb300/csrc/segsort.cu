@@ -9,8 +9,10 @@
 //              another buffer
 //   scan       exclusive scan of the tile counts of the large segments: the
 //              tiles of segment j are rows tile_base[j] .. tile_base[j+1]-1
-//   tilemap    one descriptor per tile: its segment, keys, look-back chain
-//   histogram  the 4 x 256 digit counts of every large segment
+//   tilemap    one descriptor per tile (its segment, keys, look-back chain);
+//              clears each large segment's counts
+//   histogram  the 4 x 256 digit counts of every large segment, and the
+//              first pass's look-back rows cleared
 //   4 x pass   the single-pass digit scatter of radix_kernels.cuh on tiles
 //              that never straddle a segment: bin starts come from the
 //              segment's own histogram, and the decoupled look-back of a tile
@@ -423,13 +425,29 @@ k_seg_pass_free(const PassArgs a, const SegTile *tiles, const uint32_t *counts, 
         one_digit = __all_sync(kFullMask, same);
     }
     uint32_t rk[IPT / 2];
+    uint32_t hot_base = 0;
     if (hot < 256u && !one_digit) {   // CTA-uniform
+        // keys of the hot digit rank by this warp's running count of them, and
+        // the warp reserves their slots with one atomic after the loop (their
+        // order is free); bit 15 marks such a rank until then
+        const uint32_t ltm = lanemask_lt();
+        uint32_t run = 0;
 #pragma unroll
         for (int k = 0; k < IPT; k += 2) {
-            const uint32_t r0 = take_slot_hot(s_cnt, key[k] & 0xFFu, hot, lane, k * T + tid < tile_n);
-            const uint32_t r1 = take_slot_hot(s_cnt, key[k + 1] & 0xFFu, hot, lane, (k + 1) * T + tid < tile_n);
-            rk[k / 2] = r0 | (r1 << 16);
+            uint32_t r[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const bool valid = (k + u) * T + tid < tile_n;
+                const uint32_t dg = key[k + u] & 0xFFu;
+                const bool h = valid && dg == hot;
+                const uint32_t hm = __ballot_sync(kFullMask, h);
+                r[u] = h ? (0x8000u | (run + __popc(hm & ltm))) : (valid ? atomicAdd(&s_cnt[dg], 1u) : 0u);
+                run += __popc(hm);
+            }
+            rk[k / 2] = r[0] | (r[1] << 16);
         }
+        if (lane == 0 && run != 0) hot_base = atomicAdd(&s_cnt[hot], run);
+        hot_base = __shfl_sync(kFullMask, hot_base, 0);
     } else {
 #pragma unroll
         for (int k = 0; k < IPT; k += 2) {
@@ -476,7 +494,8 @@ k_seg_pass_free(const PassArgs a, const SegTile *tiles, const uint32_t *counts, 
 #pragma unroll
     for (int k = 0; k < IPT; ++k) {
         if (k * T + tid < tile_n) {
-            const uint32_t r = (rk[k / 2] >> ((k & 1) * 16)) & 0xFFFFu;
+            uint32_t r = (rk[k / 2] >> ((k & 1) * 16)) & 0xFFFFu;
+            if (r & 0x8000u) r = hot_base + (r & 0x7FFFu);
             s_keys[s_cnt[key[k] & 0xFFu] + r] = key[k];
         }
     }
