@@ -235,44 +235,63 @@ k_seg_hist(const uint32_t *__restrict__ keys, const SegTile *tiles, const uint32
     }
     uint32_t *col = s_h + (tid & 31u);
     const bool vec = (reinterpret_cast<uintptr_t>(keys) & 15u) == 0;
-    __syncthreads();
-    for (uint32_t t = t0; t < t1;) {
+    // the piece starting at tile t: tiles t .. te-1, all of one segment, keys
+    // [a, b), the 16-byte aligned body [a4, a4 + 4 nv)
+    struct Piece {
+        uint32_t seg, te, a, b, a4, nv;
+    };
+    auto piece_at = [&](uint32_t t) {
         const SegTile d = tiles[t];
-        // the piece: tiles t .. te-1, all of segment d.seg
         const uint32_t seg_tiles = (d.out_end - d.out_base + kSegTile - 1) / kSegTile;
-        const uint32_t te = min(t1, d.first + seg_tiles);
-        const uint32_t a = d.base, b = min(d.out_end, d.base + (te - t) * kSegTile);
-        uint32_t a4 = a, b4 = a;   // the 16-byte aligned body [a4, b4)
+        Piece P;
+        P.seg = d.seg;
+        P.te = min(t1, d.first + seg_tiles);
+        P.a = d.base;
+        P.b = min(d.out_end, d.base + (P.te - t) * kSegTile);
+        P.a4 = P.a;
+        uint32_t b4 = P.a;
         if (vec) {
-            a4 = min(b, (a + 3u) & ~3u);
-            b4 = max(a4, b & ~3u);
+            P.a4 = min(P.b, (P.a + 3u) & ~3u);
+            b4 = max(P.a4, P.b & ~3u);
         }
+        P.nv = (b4 - P.a4) / 4;
+        return P;
+    };
+    // the first round of a piece's body, loaded ahead (during the previous
+    // piece's flush)
+    uint4 q[kSegHistUnroll];
+    auto load_round = [&](const Piece &P, uint32_t v) {
+        const uint4 *kv = reinterpret_cast<const uint4 *>(keys + P.a4);
+#pragma unroll
+        for (int u = 0; u < kSegHistUnroll; ++u)
+            if (v + u * T < P.nv) q[u] = __ldcs(kv + v + u * T);
+    };
+    Piece P = piece_at(t0);
+    load_round(P, tid);
+    __syncthreads();
+    while (true) {
         // the next pieces' first tiles go to L2 while this piece is counted
         // (one descriptor and one bulk prefetch per lane of the last warp)
-        if (vec && tid >= T - kSegHistAhead && te + (tid - (T - kSegHistAhead)) < t1) {
-            const SegTile dn = tiles[te + (tid - (T - kSegHistAhead))];
+        if (vec && tid >= T - kSegHistAhead && P.te + (tid - (T - kSegHistAhead)) < t1) {
+            const SegTile dn = tiles[P.te + (tid - (T - kSegHistAhead))];
             seg_hist_prefetch(keys, static_cast<uint64_t>(dn.base) * 4u, static_cast<uint64_t>(dn.base + dn.n) * 4u);
         }
-        if (tid < a4 - a) seg_hist_count<XF>(col, keys[a + tid], fmask, flip);
-        for (uint32_t i = b4 + tid; i < b; i += T) seg_hist_count<XF>(col, keys[i], fmask, flip);
-        const uint4 *kv = reinterpret_cast<const uint4 *>(keys + a4);
-        const uint32_t nv = (b4 - a4) / 4;
-        for (uint32_t v = tid; v < nv; v += T * kSegHistUnroll) {
+        const uint32_t b4 = P.a4 + 4 * P.nv;
+        if (tid < P.a4 - P.a) seg_hist_count<XF>(col, keys[P.a + tid], fmask, flip);
+        for (uint32_t i = b4 + tid; i < P.b; i += T) seg_hist_count<XF>(col, keys[i], fmask, flip);
+        for (uint32_t v = tid; v < P.nv; v += T * kSegHistUnroll) {
+            if (v != tid) load_round(P, v);   // the first round is in registers already
             if (tid == 0) {   // a long piece: its body two rounds ahead
                 const uint32_t ahead = v + 2u * T * kSegHistUnroll;   // uint4 index in the body
-                if (ahead < nv) {
-                    const uint32_t end = min(nv, ahead + T * kSegHistUnroll);
-                    seg_hist_prefetch(keys, (static_cast<uint64_t>(a4) + ahead * 4ull) * 4u,
-                                      (static_cast<uint64_t>(a4) + end * 4ull) * 4u);
+                if (ahead < P.nv) {
+                    const uint32_t end = min(P.nv, ahead + T * kSegHistUnroll);
+                    seg_hist_prefetch(keys, (static_cast<uint64_t>(P.a4) + ahead * 4ull) * 4u,
+                                      (static_cast<uint64_t>(P.a4) + end * 4ull) * 4u);
                 }
             }
-            uint4 q[kSegHistUnroll];
-#pragma unroll
-            for (int u = 0; u < kSegHistUnroll; ++u)
-                if (v + u * T < nv) q[u] = __ldcs(kv + v + u * T);
 #pragma unroll
             for (int u = 0; u < kSegHistUnroll; ++u) {
-                if (v + u * T < nv) {
+                if (v + u * T < P.nv) {
                     seg_hist_count<XF>(col, q[u].x, fmask, flip);
                     seg_hist_count<XF>(col, q[u].y, fmask, flip);
                     seg_hist_count<XF>(col, q[u].z, fmask, flip);
@@ -280,10 +299,17 @@ k_seg_hist(const uint32_t *__restrict__ keys, const SegTile *tiles, const uint32
                 }
             }
         }
+        const bool more = P.te < t1;   // uniform
+        Piece N{};
+        if (more) {   // the next piece's descriptor and first round, in flight during the flush
+            N = piece_at(P.te);
+            load_round(N, tid);
+        }
         __syncthreads();   // every count of the piece is in
-        seg_hist_flush(s_h, hist + d.seg * 1024, tid);
+        seg_hist_flush(s_h, hist + P.seg * 1024, tid);
+        if (!more) break;
         __syncthreads();
-        t = te;
+        P = N;
     }
 }
 
