@@ -141,10 +141,14 @@ __global__ void __launch_bounds__(kClusterThreads, 1) k_cluster_sort(const Clust
             }
             const uint32_t it = warp_inclusive_scan(total, lane);
             const uint32_t ic = warp_inclusive_scan(cnt, lane);
+            // the largest digit total of this warp's 32 digits, and that digit
+            const uint32_t wmax = __reduce_max_sync(kFullMask, total);
+            const uint32_t at = __ffs(__ballot_sync(kFullMask, total == wmax)) - 1;
             if (lane == 31) {
                 s_misc[4 + warp] = it;
                 s_misc[12 + warp] = ic;
             }
+            if (lane == 0) s_misc[20 + warp] = (wmax << 8) | (warp * 32 + at);   // totals < 2^17
             s_goff[tid] = it - total + before;
             cnt = ic - cnt;   // now: the exclusive scan of this tile's counts (within the warp)
         }
@@ -162,9 +166,65 @@ __global__ void __launch_bounds__(kClusterThreads, 1) k_cluster_sort(const Clust
         }
         __syncthreads();
 
-        // ---- warp multisplit: stable slot of each key in the tile-sorted
-        // order; the keys are in registers, so the input buffer is free
-        {
+        // ---- the slot of each key in the tile-sorted order; the keys are in
+        // registers, so the input buffer is free.  First pass of a keys-only
+        // sort over every bit: keys of one digit may take any order, so each
+        // takes the next free slot of its digit in its warp's range with one
+        // shared atomic (one per warp for a warp whose keys share one digit,
+        // and warp-aggregated for a digit that holds over 1/8 of the keys);
+        // otherwise the stable warp multisplit.
+        if (!PAIRS && first && a.begin_bit == 0 && a.passes == 4 && a.last_mask == 0xFFu) {
+            uint32_t hot = 256u, hmax = 0;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+                const uint32_t m = s_misc[20 + w];
+                if ((m >> 8) > hmax) {
+                    hmax = m >> 8;
+                    hot = m & 0xFFu;
+                }
+            }
+            if (hmax <= a.n / 8) hot = 256u;
+            uint32_t *wc = s_cnt + warp * kRow;
+            bool same = true;
+            const uint32_t d0 = __shfl_sync(kFullMask, digit_at<false>(key[0], shift, mask), 0);
+#pragma unroll
+            for (int k = 0; k < IPT; ++k)
+                same &= item0 + 32 * k < tile_n && digit_at<false>(key[k], shift, mask) == d0;
+            const bool one_digit = __all_sync(kFullMask, same);
+            if (hot < 256u && !one_digit) {
+                // keys of other digits take their slots; the warp counts its
+                // keys of the hot digit, reserves their slots with one atomic,
+                // then places them
+                const uint32_t ltm = lanemask_lt();
+                uint32_t run = 0;
+#pragma unroll
+                for (int k = 0; k < IPT; ++k) {
+                    const bool valid = item0 + 32 * k < tile_n;
+                    const uint32_t d = digit_at<false>(key[k], shift, mask);
+                    const bool h = valid && d == hot;
+                    run += __popc(__ballot_sync(kFullMask, h));
+                    if (valid && !h) cur_k[atomicAdd(&wc[d], 1u)] = key[k];
+                }
+                uint32_t b = 0;
+                if (lane == 0 && run != 0) b = atomicAdd(&wc[hot], run);
+                b = __shfl_sync(kFullMask, b, 0);
+#pragma unroll
+                for (int k = 0; k < IPT; ++k) {
+                    const bool h = item0 + 32 * k < tile_n && digit_at<false>(key[k], shift, mask) == hot;
+                    const uint32_t hm = __ballot_sync(kFullMask, h);
+                    if (h) cur_k[b + __popc(hm & ltm)] = key[k];
+                    b += __popc(hm);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < IPT; ++k) {
+                    const bool valid = item0 + 32 * k < tile_n;
+                    const uint32_t d = digit_at<false>(key[k], shift, mask);
+                    const uint32_t slot = one_digit ? take_slot(wc, d, lane, true) : (valid ? atomicAdd(&wc[d], 1u) : 0u);
+                    if (valid) cur_k[slot] = key[k];
+                }
+            }
+        } else {
             uint32_t *wc = s_cnt + warp * kRow;
             const uint32_t ltm = lanemask_lt();
             const LaneConsts c = lane_consts(lane);
